@@ -1,0 +1,345 @@
+"""Benchmark: attention forward TFLOPS on GB300 through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+One step = one fa_fwd launch over one batch of the workload (default: the
+non-causal B=2, H=16, N=4096, d=128 forward).  Prints one JSON line.
+
+* value: device-timed TFLOPS (4*B*H*Nq*Nk*d per step, halved when causal),
+  inputs resident in HBM, K back-to-back steps bracketed by barrier + sync,
+  rotating over enough input sets that every step's inputs exceed L2.
+* e2e: the same metric through fa_fwd_host from pinned host memory, the
+  host->device copies of Q, K, V and the device->host copies of O, LSE inside
+  the timed region.
+* roofline: the kernel's average launch time (CUDA events on its stream)
+  against the measured dense-bf16 peak; traffic from the committed ncu
+  summary when the kernel source still matches it.
+* cpu_baseline: the fp64 oracle on a bounded sample of rows, host cores.
+* --impl reference: the oracle alone, timed per step on a bounded sample.
+Under torchrun (N > 1) every rank runs its own batch (weak scaling, no
+collective on the data path); rank 0 prints the max-over-ranks result.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from exact_attention_28_gb300 import inputs  # noqa: E402
+
+METRIC = "attention fwd TFLOPS (bf16, 1 GB300) and % of dense BF16 tensor peak"
+DEFAULT_WORKLOAD = "b2_h16_n4096_d128"
+L2_BYTES = 126 * 1024 * 1024
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "fa_fwd_kernel_b2_h16_n4096_d128.txt")
+KERNEL_SOURCES = ["fa_api.cu", "fa_fwd_kernel.cuh", "ptx_sm103.cuh"]
+
+
+def env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "exact_attention_28_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """dram bytes per launch from the committed ncu summary, if still valid."""
+    try:
+        fields = {}
+        with open(PROFILE_SUMMARY, encoding="utf-8") as fh:
+            for line in fh:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        if fields.get("kernel_source_sha256") != kernel_source_hash():
+            return None
+        return float(fields["dram_bytes_per_full_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json"), encoding="utf-8") as fh:
+            return json.load(fh), "measured"
+    except (OSError, ValueError):
+        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:8]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        window = "timed region"
+        if len(inside) < 3:   # very short timed region: take the samples nearest to it
+            inside = sorted(rows, key=lambda r: abs(r[0] - 0.5 * (t0 + t1)))[:5]
+            window = "nearest samples (timed region shorter than the sampling period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+# ---------------------------------------------------------------- CPU legs
+
+def oracle_sample(w, q, k, v, target_s, nthreads):
+    """Time the oracle on a bounded row sample sized to ~target_s seconds.
+
+    Returns (TFLOPS, seconds, rows, threads)."""
+    import oracle
+    rng = np.random.default_rng(0)
+    per_row = lambda rows: sum(4 * (min(w.Nk, (r % w.Nq) + 1) if w.causal else w.Nk) * w.d for r in rows)
+    probe = rng.integers(0, w.B * w.H * w.Nq, 64)
+    t = time.perf_counter()
+    oracle.attention_rows(q, k, v, w.scale, w.causal, rows=probe, nthreads=nthreads)
+    dt = max(time.perf_counter() - t, 1e-4)
+    n = int(min(w.B * w.H * w.Nq, max(64, 64 * target_s / dt)))
+    rows = rng.integers(0, w.B * w.H * w.Nq, n)
+    t = time.perf_counter()
+    oracle.attention_rows(q, k, v, w.scale, w.causal, rows=rows, nthreads=nthreads)
+    dt = time.perf_counter() - t
+    return per_row(rows) / dt / 1e12, dt, n, nthreads
+
+
+def run_reference(args, w):
+    rank = env_int("RANK", 0)
+    if rank != 0:
+        return 0
+    q, k, v, _ = inputs.make_inputs(w)
+    cores = os.cpu_count() or 1
+    per_step = min(5.0, max(0.5, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, q, k, v, per_step, cores)
+    vals, secs, nrows = [], 0.0, 0
+    for _ in range(args.steps):
+        tf, dt, n, _ = oracle_sample(w, q, k, v, per_step, cores)
+        vals.append(tf)
+        secs += dt
+        nrows += n
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w, None),
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                         "sample": f"{nrows} rows over {args.steps} steps, fp64 three-pass oracle, "
+                                   f"{cores} threads"},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, l2_note):
+    cfg = {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": w.causal,
+           "sigma_qkv": [w.sigma_q, w.sigma_k, w.sigma_v], "scale": "1/sqrt(d) as fp32",
+           "global_batch": w.B, "seq_len": w.Nq, "parallelism": "independent replicas (weak)"}
+    if l2_note:
+        cfg["l2"] = l2_note
+    return cfg
+
+
+# -------------------------------------------------------------------- ours
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    from exact_attention_28_gb300 import build, ops
+
+    rank, world, local = env_int("RANK", 0), env_int("WORLD_SIZE", 1), env_int("LOCAL_RANK", 0)
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    build.build()
+    ops.load_library()
+
+    q, k, v, scale = inputs.make_inputs(w)
+    as_t = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    hq, hk, hv = as_t(q), as_t(k), as_t(v)
+    set_bytes = (2 * hq.numel() + 2 * hk.numel()) * 2 + w.B * w.H * w.Nq * 4
+    n_sets = max(1, math.ceil(2 * L2_BYTES / set_bytes)) if set_bytes < 2 * L2_BYTES else 1
+    sets = []
+    for _ in range(n_sets):
+        sets.append((hq.cuda(), hk.cuda(), hv.cuda(), torch.empty_like(hq, device="cuda"),
+                     torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device="cuda")))
+    l2_note = (f"rotating {n_sets} input sets, {n_sets * set_bytes / 2**20:.0f} MiB > 2x L2"
+               if n_sets > 1 else f"inputs {set_bytes / 2**20:.0f} MiB > 2x L2")
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        s = sets[i % n_sets]
+        ops.fa_fwd(s[0], s[1], s[2], s[3], s[4], scale=scale, causal=w.causal, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    ops.check_device_status()
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step(i)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        dist.barrier()
+    ops.check_device_status()
+    total_ms = starts[0].elapsed_time(ends[-1])
+    launch_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    if world > 1:
+        red = torch.tensor([total_ms, launch_ms], device="cuda")
+        dist.all_reduce(red, op=dist.ReduceOp.MAX)
+        total_ms, launch_ms = red.tolist()
+    if sampler:
+        time.sleep(0.25)
+        sampler.stop()
+
+    # end to end through the host-buffer entry point
+    pin = lambda t: t.pin_memory()
+    phq, phk, phv = pin(hq), pin(hk), pin(hv)
+    pho = torch.empty_like(hq).pin_memory()
+    phl = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32).pin_memory()
+    d = sets[0]
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        ops.fa_fwd_host(phq, phk, phv, pho, phl, *d, scale, causal=w.causal, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        ops.fa_fwd_host(phq, phk, phv, pho, phl, *d, scale, causal=w.causal, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ops.check_device_status()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        red = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(red, op=dist.ReduceOp.MAX)
+        e2e_ms = red.item()
+
+    if rank == 0:
+        peaks, peak_src = measured_peaks()
+        ms_per_step = total_ms / args.steps
+        value = world * w.flops / (ms_per_step * 1e-3) / 1e12
+        achieved = w.flops / (launch_ms * 1e-3) / 1e12
+        peak = float(peaks["bf16_tflops"])
+        traffic = profiled_traffic()
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0, sigma^2) rounded to bf16)",
+            "config": workload_config(w, l2_note),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": f"{peak_src} bf16_tflops (burst)",
+                         "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
+                         "kernel": "fa_fwd_kernel<%d>" % w.d, "launch_ms": launch_ms},
+            "e2e": {"value": world * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+                    "h2d_bytes_per_step": 3 * 0 + 2 * (hq.numel() + 2 * hk.numel()),
+                    "d2h_bytes_per_step": 2 * hq.numel() + 4 * w.B * w.H * w.Nq,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps,
+            "clocks": sampler.summary(t0, t1) if sampler else None,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            tf, dt, n, cores = oracle_sample(w, q, k, v, args.cpu_seconds, os.cpu_count() or 1)
+            line["cpu_baseline"] = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                                    "sample": f"{n} random query rows of the workload, fp64 three-pass "
+                                              f"oracle, {dt:.1f} s"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = inputs.WORKLOADS[args.workload]
+    return run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,201 @@
+// Host side of libfa_gb300.so: argument validation, TMA tensor maps, the
+// persistent schedule, and the launch.  Implements the C ABI of include/fa.h.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/fa.h"
+#include "fa_fwd_kernel.cuh"
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// so the library needs no link-time dependency on libcuda.
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// [BH][N][d] bf16, boxes of 64 columns x 128 rows x 1 head, 128-byte swizzle.
+// Rows past N inside a head read as zero (the map is 3-D, so a box never
+// spills into the next head).
+bool make_map(CUtensorMap *map, const void *ptr, int64_t BH, int64_t N, int d) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(fa::kBR), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+fa_status validate(const void *Q, const void *K, const void *V, const void *O, const float *LSE, int B,
+                   int H, int Nq, int Nk, int d, float scale) {
+    if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    // B*H heads and B*H*N*d elements must fit the kernel's index arithmetic
+    // (int heads and tiles, 64-bit element offsets) and the TMA map (< 2^32
+    // per dimension, strides < 2^40 bytes).
+    const int64_t BH = static_cast<int64_t>(B) * H;
+    if (BH > (int64_t{1} << 30)) return FA_ERR_INVALID_ARG;
+    const int64_t tiles = BH * ((static_cast<int64_t>(Nq) + 255) / 256) * 2;
+    if (tiles > (int64_t{1} << 30)) return FA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(Nq > Nk ? Nq : Nk) * d * 2 >= (int64_t{1} << 40)) return FA_ERR_INVALID_ARG;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(LSE, 4))
+        return FA_ERR_MISALIGNED;
+    return FA_OK;
+}
+
+// The work list: per head, P = ceil(Tr/2) Q-tile pairs; all pairs of all
+// heads are whole items except the last n_split (the lightest), which are
+// split into single-tile items so the last round of the persistent grid is
+// evenly filled.  Only pairs holding two tiles are split.
+void plan_schedule(fa::FwdParams &p, int grid_ctas) {
+    const int64_t BH = p.BH;
+    const int64_t NP = BH * p.P;
+    const int64_t units = BH * p.Tr;                        // Q tiles in total
+    const int64_t two_tile_pairs = BH * (p.Tr / 2);         // pairs with both tiles present
+    int64_t keep = static_cast<int64_t>(grid_ctas) * (units / (2 * static_cast<int64_t>(grid_ctas)));
+    if (keep > NP) keep = NP;
+    int64_t split = NP - keep;
+    if (split > two_tile_pairs) split = two_tile_pairs;
+    p.n_pair_items = static_cast<int>(NP - split);
+    p.n_items = static_cast<int>(NP + split);
+}
+
+struct DeviceInfo {
+    int sms = 0;
+    bool attr64 = false, attr128 = false;
+};
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+template <int D>
+fa_status launch(const fa::FwdParams &p, int grid, cudaStream_t stream, bool &attr_done) {
+    using C = fa::Config<D>;
+    if (!attr_done) {
+        if (cudaFuncSetAttribute(fa::fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::kSmemBytes) != cudaSuccess)
+            return FA_ERR_CUDA;
+        attr_done = true;
+    }
+    fa::fa_fwd_kernel<D><<<grid, fa::kThreads, C::kSmemBytes, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                            int Nq, int Nk, int d, float scale, int causal, fa_stream_t stream) {
+    fa_status st = validate(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale);
+    if (st != FA_OK) return st;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FA_ERR_CUDA;
+    int sms;
+    bool *attr_done;
+    {
+        std::lock_guard<std::mutex> lock(g_dev_mu);
+        DeviceInfo &info = g_dev[dev];
+        if (info.sms == 0 &&
+            cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return FA_ERR_CUDA;
+        sms = info.sms;
+        attr_done = d == 64 ? &info.attr64 : &info.attr128;
+    }
+
+    fa::FwdParams p;
+    std::memset(&p, 0, sizeof p);
+    const int64_t BH = static_cast<int64_t>(B) * H;
+    if (!make_map(&p.tmQ, Q, BH, Nq, d) || !make_map(&p.tmK, K, BH, Nk, d) || !make_map(&p.tmV, V, BH, Nk, d))
+        return FA_ERR_CUDA;
+    p.O = static_cast<__nv_bfloat16 *>(O);
+    p.LSE = LSE;
+    p.BH = static_cast<int>(BH);
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.Tr = (Nq + fa::kBR - 1) / fa::kBR;
+    p.Tc = (Nk + fa::kBC - 1) / fa::kBC;
+    p.P = (p.Tr + 1) / 2;
+    p.causal = causal != 0;
+    // c2 = scale * log2(e).  A zero scale is run as the smallest normal float:
+    // every score then changes by at most |S| * 2^-126, far below fp32
+    // resolution of the outputs, and masked keys keep an exact p = 0.
+    double c2 = static_cast<double>(scale) * 1.4426950408889634;
+    if (scale == 0.0f) c2 = 1.1754943508222875e-38 * 1.4426950408889634;
+    p.c2 = static_cast<float>(c2);
+    plan_schedule(p, sms);
+    const int grid = p.n_items < sms ? p.n_items : sms;
+
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    return d == 64 ? launch<64>(p, grid, reinterpret_cast<cudaStream_t>(stream), *attr_done)
+                   : launch<128>(p, grid, reinterpret_cast<cudaStream_t>(stream), *attr_done);
+}
+
+extern "C" fa_status fa_fwd_host(const void *hQ, const void *hK, const void *hV, void *hO, float *hLSE,
+                                 void *dQ, void *dK, void *dV, void *dO, float *dLSE, int B, int H, int Nq,
+                                 int Nk, int d, float scale, int causal, fa_stream_t stream) {
+    if (!hQ || !hK || !hV || !hO || !hLSE) return FA_ERR_INVALID_ARG;
+    fa_status st = validate(dQ, dK, dV, dO, dLSE, B, H, Nq, Nk, d, scale);
+    if (st != FA_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t BH = static_cast<size_t>(B) * H;
+    const size_t q_bytes = BH * Nq * d * 2, kv_bytes = BH * Nk * d * 2, lse_bytes = BH * Nq * 4;
+    if (cudaMemcpyAsync(dQ, hQ, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(dK, hK, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(dV, hV, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return FA_ERR_CUDA;
+    st = fa_fwd(dQ, dK, dV, dO, dLSE, B, H, Nq, Nk, d, scale, causal, stream);
+    if (st != FA_OK) return st;
+    if (cudaMemcpyAsync(hO, dO, q_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(hLSE, dLSE, lse_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return FA_ERR_CUDA;
+    return FA_OK;
+}
+
+extern "C" fa_status fa_check_device_status(fa_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+    unsigned int status = 0;
+    if (cudaMemcpyFromSymbol(&status, fa::g_fa_status, sizeof status) != cudaSuccess) return FA_ERR_CUDA;
+    if (status == 0) return FA_OK;
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(fa::g_fa_status, &zero, sizeof zero) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_ERR_TIMEOUT;
+}
+
+extern "C" const char *fa_status_string(fa_status s) {
+    switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: null pointer, size < 1, non-finite scale or size overflow";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dimension must be 64 or 128";
+    case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED: Q, K, V, O need 16-byte alignment, LSE 4-byte";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel wait expired; outputs are undefined";
+    }
+    return "unknown fa_status";
+}

@@ -1,0 +1,576 @@
+// FlashAttention forward for sm_103a: TMA loads, tcgen05 MMAs into tensor
+// memory (TMEM), online softmax by dedicated warpgroups, persistent CTAs.
+//
+// What is computed (per (batch, head), per query row i):
+//   S_ij = scale * q_i . k_j over the visible keys j (j < Nk; j <= i if causal)
+//   O_i  = sum_j exp(S_ij - m_i) v_j / l_i,  LSE_i = m_i + ln l_i
+// following "9.4 FlashAttention 与 FlashMLA" 9.4.2 (online softmax recurrence,
+// online update of O, O_final = O / l) and 9.4.3 (fused forward, Q-block outer
+// loop, KV-block inner loop), "6. FlashAttention 分块逻辑" 3.1-5.2 (blocked
+// loops with causal block classes), and 9.4.5 (store lse = m + log l).
+//
+// Work decomposition.  A work item is one (batch*head, Q-tile pair): two Q
+// tiles of BR = 128 rows that share every K/V tile they stream, or a single
+// Q tile for load balancing at the end of the list.  CTAs are persistent: the
+// grid is at most one CTA per SM and each CTA walks the item list with a
+// static stride, reversing direction every round ("snake") so heavy and light
+// items (causal) even out.  Items are ordered heaviest first.
+//
+// Roles inside a CTA (320 threads, 10 warps):
+//   warps 0-3  softmax for Q tile 0 (TMEM lanes 0-127: thread = query row)
+//   warps 4-7  softmax for Q tile 1
+//   warp  8    TMA producer: Q tiles once per item, then K_j, V_j into a ring
+//   warp  9    MMA issuer (one thread) and TMEM owner
+//
+// Tensor memory (512 columns x 128 lanes, fp32 cells):
+//   [  0,128)  S_0 = Q_0 K_j^T (fp32);  P_0 (bf16 pairs) overwrites its first 64 columns
+//   [128,256)  S_1 / P_1
+//   [256,256+D)      O_0 accumulator
+//   [256+D,256+2D)   O_1 accumulator
+//
+// MMA order per KV step j (tile t = 0, 1):  PV_0(j), S_0(j+1), PV_1(j), S_1(j+1).
+// While the tensor core runs the other tile's two MMAs, the softmax warps of
+// tile t turn S_t(j+1) into P_t(j+1).  Because every tcgen05.commit tracks all
+// earlier MMAs of the issuing thread, "S_t(j+1) is ready" also means PV_t(j)
+// has finished, so the softmax warps may rescale O_t in place at that point.
+//
+// Online softmax in base 2: with c = scale*log2(e), t_ij = c*S_ij and
+// p = 2^(t - m).  The reference maximum m is only raised when a tile's row
+// maximum exceeds it by more than TAU = 8 (so p <= 2^8); otherwise the O
+// rescale is skipped (alpha == 1 exactly).  The recurrence of 9.4.2 holds for
+// any reference value, so the result is unchanged; LSE = ln2 * (m + log2 l).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "ptx_sm103.cuh"
+
+namespace fa {
+
+constexpr int kBR = 128;          // query rows per Q tile (= TMEM lanes)
+constexpr int kBC = 128;          // keys per K/V tile
+constexpr int kThreads = 320;     // 10 warps
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kChunkBytes = 128 * 128;  // one [128 rows x 64 bf16] swizzled TMA box
+constexpr float kTau = 8.0f;            // log2-domain slack before the max is raised
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait, then abort
+
+// Device status word: bit 0 = a pipeline wait expired, bit 1 = a shutdown
+// wait expired.  Read and cleared by the host.
+__device__ unsigned int g_fa_status;
+// First failure: {block, role, item, step}.
+__device__ int g_fa_diag[4];
+
+template <int D>
+struct Config {
+    static_assert(D == 64 || D == 128, "head dimension");
+    static constexpr int kChunks = D / 64;                 // 128-byte swizzle chunks per row
+    static constexpr int kQTileBytes = kBR * D * 2;
+    static constexpr int kKVTileBytes = kBC * D * 2;
+    static constexpr int kSlots = (D == 128) ? 5 : 8;      // K/V ring depth (tiles)
+    static constexpr int kQBytes = 2 * kQTileBytes;
+    static constexpr int kRingBytes = kSlots * kKVTileBytes;
+    static constexpr int kBarOffset = kQBytes + kRingBytes;
+    static constexpr int kSmemBytes = kBarOffset + 256 + 1024;  // + barriers, + alignment slack
+    static constexpr uint32_t kIdescS = ptx::instr_desc_bf16_f32(kBR, kBC, false, false);
+    static constexpr uint32_t kIdescPV = ptx::instr_desc_bf16_f32(kBR, D, false, true);
+    static constexpr uint32_t kTmemCols = 512;
+};
+
+struct FwdParams {
+    CUtensorMap tmQ;   // [BH][Nq][D] bf16, box {64, 128, 1}, 128-byte swizzle
+    CUtensorMap tmK;   // [BH][Nk][D]
+    CUtensorMap tmV;   // [BH][Nk][D]
+    __nv_bfloat16 *O;  // [BH][Nq][D]
+    float *LSE;        // [BH][Nq]
+    int BH, Nq, Nk;
+    int Tr;            // Q tiles per head = ceil(Nq / 128)
+    int Tc;            // K/V tiles per head = ceil(Nk / 128)
+    int P;             // Q-tile pairs per head = ceil(Tr / 2)
+    int n_pair_items;  // items [0, n_pair_items) are whole pairs
+    int n_items;       // the rest are single tiles of the last pairs in order
+    int causal;
+    float c2;          // scale * log2(e)
+};
+
+struct Item {
+    int bh;
+    int q0;        // first query row of tile 0 of this item
+    int ntiles;    // 1 or 2
+    int nk[2];     // K/V tiles visited by each tile (0 if absent)
+};
+
+// Item w of the list: pairs ordered by descending pair index (for causal the
+// heaviest first), heads inner; the lightest pairs are split into singles.
+__device__ __forceinline__ Item decode_item(const FwdParams &p, int w) {
+    int r, first, single;
+    if (w < p.n_pair_items) {
+        r = w; first = 0; single = 0;
+    } else {
+        const int s = w - p.n_pair_items;
+        r = p.n_pair_items + (s >> 1); first = s & 1; single = 1;
+    }
+    const int pair = p.P - 1 - r / p.BH;
+    Item it;
+    it.bh = r % p.BH;
+    it.q0 = (2 * pair + first) * kBR;
+    const int left = p.Tr - (2 * pair + first);
+    it.ntiles = single ? 1 : (left >= 2 ? 2 : 1);
+    #pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        int nk = 0;
+        if (t < it.ntiles) {
+            nk = p.Tc;
+            if (p.causal) {
+                const int q_end = min(p.Nq, it.q0 + (t + 1) * kBR);  // rows >= Nq are padding
+                nk = min(p.Tc, (q_end - 1) / kBC + 1);
+            }
+        }
+        it.nk[t] = nk;
+    }
+    return it;
+}
+
+// Item index of round k for this CTA (snake order), or -1 when done.
+__device__ __forceinline__ int item_of_round(const FwdParams &p, int k) {
+    const int G = gridDim.x;
+    const int b = blockIdx.x;
+    const int w = k * G + ((k & 1) ? (G - 1 - b) : b);
+    return w < p.n_items ? w : -1;
+}
+
+struct Shared {
+    uint32_t q_full, q_empty;
+    uint32_t kv_full0, kv_empty0;  // + 8 * slot
+    uint32_t s_full0, p_full0, o_full0;  // + 8 * tile
+    uint32_t done;
+    volatile int *abort_flag;
+};
+
+// Bounded wait: true when the phase completed; false after the time limit
+// or when another warp of this CTA has aborted.
+__device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                       int role, int item, int step) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((n & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                if (atomicOr(&g_fa_status, 1u) == 0u) {
+                    g_fa_diag[0] = blockIdx.x; g_fa_diag[1] = role;
+                    g_fa_diag[2] = item; g_fa_diag[3] = step;
+                }
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                         int role, int item, int step) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, abort_flag, role, item, step);
+}
+
+// Bounded wait used while shutting down: ignores the abort flag (copies and
+// MMAs already started must still be waited for), gives up after the limit.
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((n & 63u) == 0 && ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(&g_fa_status, 2u);
+            return false;
+        }
+    }
+}
+
+// ------------------------------------------------------------ producer warp
+
+template <int D>
+__device__ void producer_role(const FwdParams &p, const Shared &sh, uint32_t smem_q,
+                              uint32_t smem_ring, uint32_t &loads_issued, uint32_t &q_arms) {
+    using C = Config<D>;
+    const uint64_t pol_q = ptx::l2_policy_evict_first();
+    const uint64_t pol_kv = ptx::l2_policy_evict_last();
+    uint32_t it = 0;
+    for (int k = 0;; ++k) {
+        const int w = item_of_round(p, k);
+        if (w < 0) break;
+        const Item item = decode_item(p, w);
+        if (k > 0 && !wait_bar(sh.q_empty, (k - 1) & 1, sh.abort_flag, 0, w, -1)) break;
+        ptx::mbar_arrive_expect_tx(sh.q_full, item.ntiles * C::kQTileBytes);
+        ++q_arms;
+        for (int t = 0; t < item.ntiles; ++t)
+            #pragma unroll
+            for (int c = 0; c < C::kChunks; ++c)
+                ptx::tma_load_3d(smem_q + t * C::kQTileBytes + c * kChunkBytes, &p.tmQ, sh.q_full,
+                                 c * 64, item.q0 + t * kBR, item.bh, pol_q);
+        const int nkv = max(item.nk[0], item.nk[1]);
+        bool ok = true;
+        for (int j = 0; j < nkv && ok; ++j) {
+            #pragma unroll 1
+            for (int which = 0; which < 2; ++which, ++it) {
+                const uint32_t slot = it % C::kSlots;
+                const uint32_t use = it / C::kSlots;
+                if (!wait_bar(sh.kv_empty0 + 8 * slot, (use & 1) ^ 1, sh.abort_flag, 0, w, j)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t full = sh.kv_full0 + 8 * slot;
+                ptx::mbar_arrive_expect_tx(full, C::kKVTileBytes);
+                const CUtensorMap *map = which ? &p.tmV : &p.tmK;
+                #pragma unroll
+                for (int c = 0; c < C::kChunks; ++c)
+                    ptx::tma_load_3d(smem_ring + slot * C::kKVTileBytes + c * kChunkBytes, map, full,
+                                     c * 64, j * kBC, item.bh, pol_kv);
+                loads_issued = it + 1;
+            }
+        }
+        if (!ok) break;
+    }
+}
+
+// ----------------------------------------------------------------- MMA warp
+
+template <int D>
+__device__ __forceinline__ void issue_s(uint32_t tmem_s, uint32_t q_tile, uint32_t k_tile) {
+    using C = Config<D>;
+    #pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+        const uint64_t a = ptx::smem_desc_sw128(q_tile + off, 16, 1024);
+        const uint64_t b = ptx::smem_desc_sw128(k_tile + off, 16, 1024);
+        ptx::mma_bf16_ss(tmem_s, a, b, C::kIdescS, kk > 0 ? 1u : 0u);
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_tile,
+                                         bool accumulate) {
+    using C = Config<D>;
+    #pragma unroll
+    for (int kk = 0; kk < kBC / 16; ++kk) {
+        // V tile: [128 keys][D] as D/64 boxes of [128][64]; the B operand is
+        // MN-major (D contiguous): 8-key groups SBO = 1024 B apart, 64-column
+        // groups LBO = one box (16 KB) apart; 16 keys per MMA step.
+        const uint64_t b = ptx::smem_desc_sw128(v_tile + kk * 16 * 128, kChunkBytes, 1024);
+        ptx::mma_bf16_ts(tmem_o, tmem_p + kk * 8, b, C::kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+    }
+}
+
+template <int D>
+__device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, uint32_t smem_q,
+                         uint32_t smem_ring) {
+    using C = Config<D>;
+    uint32_t it = 0;
+    uint32_t p_phase[2] = {0u, 0u};
+    const uint32_t tS[2] = {tmem + 0u, tmem + 128u};
+    const uint32_t tO[2] = {tmem + 256u, tmem + 256u + D};
+    const uint32_t sQ[2] = {smem_q, smem_q + C::kQTileBytes};
+    for (int k = 0;; ++k) {
+        const int w = item_of_round(p, k);
+        if (w < 0) break;
+        const Item item = decode_item(p, w);
+        const int nk0 = item.nk[0], nk1 = item.nk[1];
+        const int nkv = max(nk0, nk1);
+        if (!wait_bar(sh.q_full, k & 1, sh.abort_flag, 1, w, -1)) return;
+        ptx::tc_fence_after_sync();
+
+        // S_t(0) for both tiles from K_0.
+        uint32_t ks = it % C::kSlots;
+        if (!wait_bar(sh.kv_full0 + 8 * ks, (it / C::kSlots) & 1, sh.abort_flag, 1, w, 0)) return;
+        ptx::tc_fence_after_sync();
+        for (int t = 0; t < 2; ++t) {
+            if (item.nk[t] > 0) {
+                issue_s<D>(tS[t], sQ[t], smem_ring + ks * C::kKVTileBytes);
+                ptx::mma_commit(sh.s_full0 + 8 * t);
+            }
+        }
+        ptx::mma_commit(sh.kv_empty0 + 8 * ks);
+        if (nkv == 1) ptx::mma_commit(sh.q_empty);
+        ++it;
+
+        for (int j = 0; j < nkv; ++j) {
+            const uint32_t vs = it % C::kSlots;
+            if (!wait_bar(sh.kv_full0 + 8 * vs, (it / C::kSlots) & 1, sh.abort_flag, 1, w, j)) return;
+            ptx::tc_fence_after_sync();
+            ++it;
+            const uint32_t v_tile = smem_ring + vs * C::kKVTileBytes;
+            const bool more = j + 1 < nkv;
+            const uint32_t ks2 = it % C::kSlots;
+
+            if (j < nk0) {
+                if (!wait_bar(sh.p_full0, p_phase[0], sh.abort_flag, 1, w, j)) return;
+                p_phase[0] ^= 1u;
+                ptx::tc_fence_after_sync();
+                issue_pv<D>(tO[0], tS[0], v_tile, j > 0);
+                if (j == nk0 - 1) ptx::mma_commit(sh.o_full0);
+            }
+            if (more) {
+                if (!wait_bar(sh.kv_full0 + 8 * ks2, (it / C::kSlots) & 1, sh.abort_flag, 1, w, j + 1))
+                    return;
+                ptx::tc_fence_after_sync();
+                if (j + 1 < nk0) {
+                    issue_s<D>(tS[0], sQ[0], smem_ring + ks2 * C::kKVTileBytes);
+                    ptx::mma_commit(sh.s_full0);
+                }
+            }
+            if (j < nk1) {
+                if (!wait_bar(sh.p_full0 + 8, p_phase[1], sh.abort_flag, 1, w, j)) return;
+                p_phase[1] ^= 1u;
+                ptx::tc_fence_after_sync();
+                issue_pv<D>(tO[1], tS[1], v_tile, j > 0);
+                if (j == nk1 - 1) ptx::mma_commit(sh.o_full0 + 8);
+            }
+            ptx::mma_commit(sh.kv_empty0 + 8 * vs);
+            if (more) {
+                if (j + 1 < nk1) {
+                    issue_s<D>(tS[1], sQ[1], smem_ring + ks2 * C::kKVTileBytes);
+                    ptx::mma_commit(sh.s_full0 + 8);
+                }
+                ptx::mma_commit(sh.kv_empty0 + 8 * ks2);
+                if (j + 2 == nkv) ptx::mma_commit(sh.q_empty);
+                ++it;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------ softmax warps
+
+// P for one S tile held in registers (thread = row): p = 2^(c*s - m) for
+// each key, packed to bf16 pairs and written over the first 64 columns of the
+// S tile in TMEM, 32 keys at a time so few packed registers are live.
+// Masked keys already hold -inf*sign(c) and come out as p = 0.
+// Returns the row sum of the fp32 p values.
+__device__ __forceinline__ float exp_pack_store(const uint32_t (&s)[128], float c2, float neg_m,
+                                                uint32_t tP) {
+    float acc0 = 0.f, acc1 = 0.f;
+    #pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t pk[16];
+        #pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int c = 32 * q + 2 * i;
+            const float p0 = ptx::ex2(fmaf(__uint_as_float(s[c]), c2, neg_m));
+            const float p1 = ptx::ex2(fmaf(__uint_as_float(s[c + 1]), c2, neg_m));
+            acc0 += p0;
+            acc1 += p1;
+            pk[i] = ptx::pack_bf16x2(p0, p1);
+        }
+        ptx::tmem_store_16cols(tP + 16 * q, pk);
+    }
+    return acc0 + acc1;
+}
+
+template <int D>
+__device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem, int tile,
+                             int quad, int lane) {
+    const int row = quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_off + tile * 128;
+    const uint32_t tO = tmem + lane_off + 256 + tile * D;
+    const float c2 = p.c2;
+    // A masked key must never win the row extreme and must give p = 0:
+    // -inf for a positive scale, +inf for a negative one (the host never
+    // passes c2 == 0, see fa_fwd).
+    const float mask_val = c2 > 0.f ? -INFINITY : INFINITY;
+    uint32_t s_phase = 0, o_phase = 0;
+
+    for (int k = 0;; ++k) {
+        const int w = item_of_round(p, k);
+        if (w < 0) break;
+        const Item item = decode_item(p, w);
+        if (tile >= item.ntiles) continue;
+        const int nk = item.nk[tile];
+        const int qg = item.q0 + tile * kBR + row;   // this thread's query row
+        const int key_lim = p.causal ? min(p.Nk, qg + 1) : p.Nk;
+        float m_ref = -INFINITY;   // log2-domain reference maximum
+        float l = 0.f;
+
+        for (int j = 0; j < nk; ++j) {
+            if (!wait_bar(sh.s_full0 + 8 * tile, s_phase, sh.abort_flag, 2 + tile, w, j)) return;
+            s_phase ^= 1u;
+            ptx::tc_fence_after_sync();
+            uint32_t s[128];
+            ptx::tmem_load_128cols(tS, s);
+
+            const int kvalid = key_lim - j * kBC;
+            const bool masked = __any_sync(0xffffffffu, kvalid < kBC);   // warp-uniform path
+            if (masked) {
+                #pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (c >= kvalid) s[c] = __float_as_uint(mask_val);
+            }
+            float mx;
+            if (c2 > 0.f) {
+                float a = __uint_as_float(s[0]), b = __uint_as_float(s[1]);
+                #pragma unroll
+                for (int c = 2; c < 128; c += 2) {
+                    a = fmaxf(a, __uint_as_float(s[c]));
+                    b = fmaxf(b, __uint_as_float(s[c + 1]));
+                }
+                mx = fmaxf(a, b);
+            } else {
+                float a = __uint_as_float(s[0]), b = __uint_as_float(s[1]);
+                #pragma unroll
+                for (int c = 2; c < 128; c += 2) {
+                    a = fminf(a, __uint_as_float(s[c]));
+                    b = fminf(b, __uint_as_float(s[c + 1]));
+                }
+                mx = fminf(a, b);
+            }
+            const float m_tile = kvalid > 0 ? mx * c2 : -INFINITY;
+            float alpha = 1.f;
+            if (m_tile > m_ref + kTau) {
+                alpha = ptx::ex2(m_ref - m_tile);   // 0 on the first visible tile
+                m_ref = m_tile;
+            }
+            l *= alpha;
+
+            // m_ref is finite once a row has seen a key (every row sees key 0
+            // in its first tile); the guard keeps a fully masked row at p = 0.
+            l += exp_pack_store(s, c2, m_ref == -INFINITY ? 0.f : -m_ref, tS);
+            // Rescale O_t in TMEM when this warp's reference maximum moved
+            // (PV_t(j-1) has completed, see the header; PV_t(j) waits for us).
+            if (__any_sync(0xffffffffu, j > 0 && alpha != 1.f)) {
+                #pragma unroll 1
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t o[32];
+                    ptx::tmem_load_32cols(tO + ch * 32, o);
+                    #pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    ptx::tmem_store_32cols(tO + ch * 32, o);
+                }
+            }
+            ptx::tmem_wait_store();
+            ptx::tc_fence_before_sync();
+            ptx::mbar_arrive(sh.p_full0 + 8 * tile);
+        }
+
+        // Epilogue: O = O / l in bf16, LSE = ln2 * (m + log2 l).
+        if (!wait_bar(sh.o_full0 + 8 * tile, o_phase, sh.abort_flag, 2 + tile, w, nk)) return;
+        o_phase ^= 1u;
+        ptx::tc_fence_after_sync();
+        const float inv_l = 1.f / l;
+        const bool live = qg < p.Nq;
+        __nv_bfloat16 *orow = p.O + (static_cast<size_t>(item.bh) * p.Nq + qg) * D;
+        #pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t o[32];
+            ptx::tmem_load_32cols(tO + ch * 32, o);
+            uint32_t h[16];
+            #pragma unroll
+            for (int i = 0; i < 16; ++i)
+                h[i] = ptx::pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
+                                        __uint_as_float(o[2 * i + 1]) * inv_l);
+            if (live) {
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
+                #pragma unroll
+                for (int i = 0; i < 4; ++i) dst[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+            }
+        }
+        if (live)
+            p.LSE[static_cast<size_t>(item.bh) * p.Nq + qg] = (m_ref + ptx::lg2(l)) * 0.69314718055994531f;
+        ptx::tc_fence_before_sync();
+    }
+}
+
+// ------------------------------------------------------------------- kernel
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+    using C = Config<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte alignment for the 128-byte-swizzled operand tiles.
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *base_ptr = smem_raw + (base - raw);
+    const uint32_t smem_q = base;
+    const uint32_t smem_ring = base + C::kQBytes;
+    const uint32_t bars = base + C::kBarOffset;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(base_ptr + C::kBarOffset + 200);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base_ptr + C::kBarOffset + 208);
+
+    Shared sh;
+    sh.q_full = bars + 0;
+    sh.q_empty = bars + 8;
+    sh.s_full0 = bars + 16;       // 2 barriers
+    sh.p_full0 = bars + 32;       // 2
+    sh.o_full0 = bars + 48;       // 2
+    sh.done = bars + 64;
+    sh.kv_full0 = bars + 72;      // kSlots
+    sh.kv_empty0 = bars + 72 + 8 * C::kSlots;
+    sh.abort_flag = abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(sh.q_full, 1);
+        ptx::mbar_init(sh.q_empty, 1);
+        for (int t = 0; t < 2; ++t) {
+            ptx::mbar_init(sh.s_full0 + 8 * t, 1);
+            ptx::mbar_init(sh.p_full0 + 8 * t, 128);
+            ptx::mbar_init(sh.o_full0 + 8 * t, 1);
+        }
+        ptx::mbar_init(sh.done, 1);
+        for (int s = 0; s < C::kSlots; ++s) {
+            ptx::mbar_init(sh.kv_full0 + 8 * s, 1);
+            ptx::mbar_init(sh.kv_empty0 + 8 * s, 1);
+        }
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        ptx::prefetch_tensormap(&p.tmQ);
+        ptx::prefetch_tensormap(&p.tmK);
+        ptx::prefetch_tensormap(&p.tmV);
+    }
+    if (warp == kMmaWarp) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_holder), C::kTmemCols);
+        ptx::tmem_relinquish_alloc_permit();
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem = *tmem_holder;
+
+    uint32_t loads_issued = 0, q_arms = 0;
+    if (warp < 8) {
+        softmax_role<D>(p, sh, tmem, warp >> 2, warp & 3, lane);
+    } else if (warp == kProducerWarp) {
+        if (lane == 0) {
+            producer_role<D>(p, sh, smem_q, smem_ring, loads_issued, q_arms);
+            // Drain: every copy this CTA started must land before it exits.
+            const uint32_t first = loads_issued > (uint32_t)C::kSlots ? loads_issued - C::kSlots : 0u;
+            for (uint32_t x = first; x < loads_issued; ++x)
+                wait_drain(sh.kv_full0 + 8 * (x % C::kSlots), (x / C::kSlots) & 1);
+            if (q_arms > 0) wait_drain(sh.q_full, (q_arms - 1) & 1);
+        }
+        __syncwarp();
+    } else {
+        if (lane == 0) mma_role<D>(p, sh, tmem, smem_q, smem_ring);
+        __syncwarp();
+    }
+
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        if (lane == 0) {
+            // All MMAs this thread issued must finish before TMEM is released.
+            ptx::mma_commit(sh.done);
+            wait_drain(sh.done, 0);
+        }
+        __syncwarp();
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+}  // namespace fa

@@ -1,0 +1,112 @@
+"""ctypes binding of libfa_gb300.so: the C entry points under the same names.
+
+Argument marshalling only -- every step of the computation runs in the CUDA
+library.  There is no fallback: a missing library or a failing call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(6)
+
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+def load_library(path: str | None = None):
+    """Load the compiled library (build it first with __graft_entry__.build())."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise FileNotFoundError(
+            f"{path} is missing: the CUDA library has not been built (run __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd.restype = i
+    lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd_host.restype = i
+    lib.fa_check_device_status.argtypes = [vp]
+    lib.fa_check_device_status.restype = i
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().fa_status_string(status).decode()
+
+
+def _check(status: int):
+    if status != FA_OK:
+        raise FAError(status, status_string(status))
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(getattr(stream, "cuda_stream", stream))
+
+
+def _shape(q, k):
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    return B, H, Nq, Nk, d
+
+
+def fa_fwd(q, k, v, o=None, lse=None, scale=None, causal=False, stream=None):
+    """O, LSE = attention(q, k, v) on the GPU through the C ABI.
+
+    q: bf16 [B,H,Nq,d], k/v: bf16 [B,H,Nk,d], contiguous CUDA tensors.
+    Returns (o, lse); o bf16 [B,H,Nq,d], lse fp32 [B,H,Nq].
+    """
+    for t in (q, k, v):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()):
+            raise TypeError("q, k, v must be contiguous bf16 CUDA tensors")
+    B, H, Nq, Nk, d = _shape(q, k)
+    if k.shape != (B, H, Nk, d) or v.shape != (B, H, Nk, d):
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)} k {tuple(k.shape)} v {tuple(v.shape)}")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _check(load_library().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                 B, H, Nq, Nk, d, scale, int(bool(causal)), _stream_handle(stream)))
+    return o, lse
+
+
+def fa_fwd_host(hq, hk, hv, ho, hlse, dq, dk, dv, do, dlse, scale, causal=False, stream=None):
+    """End-to-end call from (pinned) host tensors through caller-owned device buffers."""
+    B, H, Nq, Nk, d = _shape(hq, hk)
+    _check(load_library().fa_fwd_host(hq.data_ptr(), hk.data_ptr(), hv.data_ptr(), ho.data_ptr(),
+                                      hlse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                      do.data_ptr(), dlse.data_ptr(), B, H, Nq, Nk, d, scale,
+                                      int(bool(causal)), _stream_handle(stream)))
+
+
+def check_device_status(stream=None):
+    """Synchronise and raise if a kernel of the library hit a wait limit."""
+    _check(load_library().fa_check_device_status(_stream_handle(stream)))
+
+
+def raw_fa_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Nq, Nk, d, scale, causal, stream_handle=0) -> int:
+    """The C call with raw integers; returns the status code (argument tests)."""
+    return load_library().fa_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Nq, Nk, d, scale,
+                                 int(causal), stream_handle)

@@ -1,0 +1,101 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) FlashAttention forward library
+ * (libfa_gb300.so).
+ *
+ * The operation is exact softmax attention computed tile by tile with the
+ * online-softmax running maximum and running sum, so the N x N score matrix
+ * never reaches HBM:
+ *
+ *   S = scale * Q K^T,   P = softmax(S) row-wise (over the visible keys),
+ *   O = P V,             LSE_i = m_i + ln(l_i)  (log-sum-exp of row i of S)
+ *
+ * Definitions followed:
+ *   - "9.4 FlashAttention 与 FlashMLA", sections 9.4.2 (online softmax
+ *     recurrence and the online update of O) and 9.4.3 (the fused forward
+ *     pass), 9.4.5 (the forward also stores lse = m + log(l));
+ *   - "6. FlashAttention 分块逻辑", sections 3.1 (Q-block / KV-block loops,
+ *     S = Q K^T * scale), 3.3 and 9 ([B,H,N,d] handled as B*H independent
+ *     sequences), 4.1-4.2 (causal mask: key j visible to query i iff j <= i);
+ *   - "08. Triton Flash Attention", Step 4 (the wrapper that takes q, k, v and
+ *     sm_scale and returns the attention output).
+ *
+ * All entry points are plain C: pointers, sizes, a stream handle.  Nothing is
+ * thrown across the ABI and no error state is kept between calls, except the
+ * device-side status word described at fa_check_device_status().
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t / CUstream); NULL is the legacy default stream. */
+typedef struct CUstream_st *fa_stream_t;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,  /* null pointer, a size < 1, non-finite scale, size overflow */
+    FA_ERR_UNSUPPORTED = 2,  /* head dimension d other than 64 or 128 */
+    FA_ERR_MISALIGNED = 3,   /* Q, K, V or O not 16-byte aligned, or LSE not 4-byte aligned */
+    FA_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed (launch, copy, encode) */
+    FA_ERR_TIMEOUT = 5       /* a kernel wait ran past its limit (see fa_check_device_status) */
+} fa_status;
+
+/*
+ * fa_fwd -- attention forward on device buffers.
+ *
+ *   Q    bf16 [B, H, Nq, d]   contiguous row-major, device memory, read only
+ *   K    bf16 [B, H, Nk, d]   contiguous row-major, device memory, read only
+ *   V    bf16 [B, H, Nk, d]   contiguous row-major, device memory, read only
+ *   O    bf16 [B, H, Nq, d]   output, device memory, fully overwritten
+ *   LSE  fp32 [B, H, Nq]      output, device memory: ln sum_j exp(S_ij) per row
+ *   B, H, Nq, Nk >= 1;  d in {64, 128};  scale finite (1/sqrt(d) is usual)
+ *   causal != 0: key j is visible to query i iff j <= i, with absolute indices
+ *                (top-left alignment; every row sees key 0, so none is empty)
+ *   stream: the work is enqueued on this stream and the call returns at once.
+ *
+ * Ownership: every pointer is caller-owned; the library allocates nothing and
+ * keeps no pointer after returning.  Q, K, V must not overlap O or LSE.
+ * Inputs are assumed finite; NaN or Inf in Q, K or V gives undefined output.
+ *
+ * Errors are reported before anything is enqueued, except FA_ERR_CUDA from the
+ * launch itself.  A wait inside the kernel that runs past its limit does not
+ * hang the GPU: the kernel stops, records the fact in a device status word and
+ * the outputs are undefined; fa_check_device_status() reports it.
+ */
+fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                 int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                 fa_stream_t stream);
+
+/*
+ * fa_fwd_host -- the same operation end to end from host memory: copies hQ,
+ * hK, hV to the caller's device buffers dQ, dK, dV, runs fa_fwd, and copies
+ * dO, dLSE back to hO, hLSE, all enqueued on `stream` in that order.  Host
+ * buffers should be pinned (page-locked) for the copies to be asynchronous.
+ * Shapes, layouts, alignment and errors are those of fa_fwd; the call does
+ * not wait for completion (synchronise the stream before reading hO, hLSE).
+ */
+fa_status fa_fwd_host(const void *hQ, const void *hK, const void *hV, void *hO, float *hLSE,
+                      void *dQ, void *dK, void *dV, void *dO, float *dLSE,
+                      int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                      fa_stream_t stream);
+
+/*
+ * fa_check_device_status -- synchronises `stream`, then reads and clears the
+ * device status word that kernels of this library set when one of their
+ * bounded waits expires.  Returns FA_OK, FA_ERR_TIMEOUT, or FA_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+fa_status fa_check_device_status(fa_stream_t stream);
+
+/* A static, human-readable name for a status code (never NULL). */
+const char *fa_status_string(fa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,97 @@
+"""The C-ABI library: it loads, exports what include/fa.h declares, and
+rejects bad arguments on the host before touching the GPU."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import __graft_entry__  # noqa: F401  (puts the repo root on sys.path)
+from exact_attention_28_gb300 import build, ops
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return ops.load_library()
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"fa_fwd", "fa_fwd_host", "fa_check_device_status", "fa_status_string"} <= set(names)
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_binding_matches_header_arity(lib):
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER, encoding="utf-8").read(), flags=re.S)
+    for name in declared_functions():
+        m = re.search(rf"\b{name}\s*\(([^)]*)\)", text)
+        nparams = 0 if m.group(1).strip() in ("", "void") else m.group(1).count(",") + 1
+        assert len(getattr(lib, name).argtypes) == nparams, name
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert ops.status_string(s)
+    assert "unknown" in ops.status_string(99)
+
+
+GOOD = dict(q=0x10000, k=0x20000, v=0x30000, o=0x40000, lse=0x50000,
+            B=1, H=1, Nq=4, Nk=4, d=64, scale=0.125, causal=0)
+
+
+def call(**kw):
+    a = dict(GOOD, **kw)
+    return ops.raw_fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"], a["Nk"],
+                          a["d"], a["scale"], a["causal"])
+
+
+@pytest.mark.parametrize("kw,expected", [
+    (dict(q=0), ops.FA_ERR_INVALID_ARG),
+    (dict(k=0), ops.FA_ERR_INVALID_ARG),
+    (dict(v=0), ops.FA_ERR_INVALID_ARG),
+    (dict(o=0), ops.FA_ERR_INVALID_ARG),
+    (dict(lse=0), ops.FA_ERR_INVALID_ARG),
+    (dict(B=0), ops.FA_ERR_INVALID_ARG),
+    (dict(H=-1), ops.FA_ERR_INVALID_ARG),
+    (dict(Nq=0), ops.FA_ERR_INVALID_ARG),
+    (dict(Nk=0), ops.FA_ERR_INVALID_ARG),
+    (dict(scale=math.nan), ops.FA_ERR_INVALID_ARG),
+    (dict(scale=math.inf), ops.FA_ERR_INVALID_ARG),
+    (dict(d=96), ops.FA_ERR_UNSUPPORTED),
+    (dict(d=32), ops.FA_ERR_UNSUPPORTED),     # the smallest test shape on the Triton page
+    (dict(d=256), ops.FA_ERR_UNSUPPORTED),
+    (dict(q=0x10008), ops.FA_ERR_MISALIGNED),
+    (dict(o=0x40002), ops.FA_ERR_MISALIGNED),
+    (dict(lse=0x50002), ops.FA_ERR_MISALIGNED),
+    (dict(B=1 << 16, H=1 << 16), ops.FA_ERR_INVALID_ARG),   # B*H overflow
+])
+def test_argument_errors_before_any_launch(lib, kw, expected):
+    assert call(**kw) == expected
+
+
+def test_host_entry_rejects_null_host_buffers(lib):
+    vp = ctypes.c_void_p
+    st = lib.fa_fwd_host(None, vp(1 << 16), vp(1 << 16), vp(1 << 16), vp(1 << 16),
+                         vp(1 << 16), vp(1 << 16), vp(1 << 16), vp(1 << 16), vp(1 << 16),
+                         1, 1, 4, 4, 64, 0.125, 0, None)
+    assert st == ops.FA_ERR_INVALID_ARG
+
+
+def test_no_gpu_means_cuda_error_not_a_fallback(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # Valid arguments on a machine without a GPU: the call must fail loudly.
+    assert call() == ops.FA_ERR_CUDA
