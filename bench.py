@@ -205,6 +205,28 @@ def workload_config(w, l2_note):
 
 # -------------------------------------------------------------------- ours
 
+def run_e2e(args, w, hq, hk, hv, dev_set, scale, stream):
+    """ms per step of fa_fwd_host from pinned host buffers (copies included)."""
+    import torch
+
+    from exact_attention_28_gb300 import ops
+    phq, phk, phv = hq.pin_memory(), hk.pin_memory(), hv.pin_memory()
+    pho = torch.empty_like(hq).pin_memory()
+    phl = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        ops.fa_fwd_host(phq, phk, phv, pho, phl, *dev_set, scale, causal=w.causal, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        ops.fa_fwd_host(phq, phk, phv, pho, phl, *dev_set, scale, causal=w.causal, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ops.check_device_status()
+    return e0.elapsed_time(e1) / e2e_steps
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -268,28 +290,13 @@ def run_ours(args, w):
         sampler.stop()
 
     # end to end through the host-buffer entry point
-    pin = lambda t: t.pin_memory()
-    phq, phk, phv = pin(hq), pin(hk), pin(hv)
-    pho = torch.empty_like(hq).pin_memory()
-    phl = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32).pin_memory()
-    d = sets[0]
-    e2e_steps = max(3, min(args.steps, 20))
-    for _ in range(2):
-        ops.fa_fwd_host(phq, phk, phv, pho, phl, *d, scale, causal=w.causal, stream=stream)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        ops.fa_fwd_host(phq, phk, phv, pho, phl, *d, scale, causal=w.causal, stream=stream)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ops.check_device_status()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
+    e2e_ms = float("nan")
+    if not args.no_e2e:
+        e2e_ms = run_e2e(args, w, hq, hk, hv, sets[0], scale, stream)
+    if world > 1 and not args.no_e2e:
         red = torch.tensor([e2e_ms], device="cuda")
         dist.all_reduce(red, op=dist.ReduceOp.MAX)
         e2e_ms = red.item()
-
     if rank == 0:
         peaks, peak_src = measured_peaks()
         ms_per_step = total_ms / args.steps
@@ -307,10 +314,11 @@ def run_ours(args, w):
                          "peak_source": f"{peak_src} bf16_tflops (burst)",
                          "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
                          "kernel": "fa_fwd_kernel<%d>" % w.d, "launch_ms": launch_ms},
-            "e2e": {"value": world * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
-                    "h2d_bytes_per_step": 3 * 0 + 2 * (hq.numel() + 2 * hk.numel()),
-                    "d2h_bytes_per_step": 2 * hq.numel() + 4 * w.B * w.H * w.Nq,
-                    "ms_per_step": e2e_ms},
+            "e2e": None if args.no_e2e else {
+                "value": world * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+                "h2d_bytes_per_step": 2 * (hq.numel() + 2 * hk.numel()),
+                "d2h_bytes_per_step": 2 * hq.numel() + 4 * w.B * w.H * w.Nq,
+                "ms_per_step": e2e_ms},
             "gpu_launches": args.steps,
             "clocks": sampler.summary(t0, t1) if sampler else None,
         }
@@ -328,12 +336,13 @@ def run_ours(args, w):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -16,11 +16,15 @@
 // static stride, reversing direction every round ("snake") so heavy and light
 // items (causal) even out.  Items are ordered heaviest first.
 //
-// Roles inside a CTA (320 threads, 10 warps):
-//   warps 0-3  softmax for Q tile 0 (TMEM lanes 0-127: thread = query row)
-//   warps 4-7  softmax for Q tile 1
-//   warp  8    TMA producer: Q tiles once per item, then K_j, V_j into a ring
-//   warp  9    MMA issuer (one thread) and TMEM owner
+// Roles inside a CTA (384 threads, 3 warpgroups):
+//   warps 0-3   softmax for Q tile 0 (TMEM lanes 0-127: thread = query row)
+//   warps 4-7   softmax for Q tile 1
+//   warp  8     TMA producer: Q tiles once per item, then K_j, V_j into a ring
+//   warp  9     MMA issuer (one thread) and TMEM owner
+//   warps 10-11 idle (they complete the third warpgroup)
+// The softmax warpgroups raise their register limit to 208 (128 scores per
+// thread plus room for many exponentials in flight); the third warpgroup
+// lowers its own to 88.
 //
 // Tensor memory (512 columns x 128 lanes, fp32 cells):
 //   [  0,128)  S_0 = Q_0 K_j^T (fp32);  P_0 (bf16 pairs) overwrites its first 64 columns
@@ -51,9 +55,13 @@ namespace fa {
 
 constexpr int kBR = 128;          // query rows per Q tile (= TMEM lanes)
 constexpr int kBC = 128;          // keys per K/V tile
-constexpr int kThreads = 320;     // 10 warps
+constexpr int kThreads = 384;     // 12 warps = 3 warpgroups
+constexpr int kSoftmaxWarps = 8;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr uint32_t kSoftmaxRegs = 208;  // after setmaxnreg; launch gives 168
+constexpr uint32_t kOtherRegs = 88;     // producer / MMA warpgroup
+static_assert(kSoftmaxRegs * 256 + kOtherRegs * 128 <= 168 * kThreads, "register split exceeds the launch allocation");
 constexpr int kChunkBytes = 128 * 128;  // one [128 rows x 64 bf16] swizzled TMA box
 constexpr float kTau = 8.0f;            // log2-domain slack before the max is raised
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait, then abort
@@ -75,6 +83,7 @@ struct Config {
     static constexpr int kRingBytes = kSlots * kKVTileBytes;
     static constexpr int kBarOffset = kQBytes + kRingBytes;
     static constexpr int kSmemBytes = kBarOffset + 256 + 1024;  // + barriers, + alignment slack
+    static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
     static constexpr uint32_t kIdescS = ptx::instr_desc_bf16_f32(kBR, kBC, false, false);
     static constexpr uint32_t kIdescPV = ptx::instr_desc_bf16_f32(kBR, D, false, true);
     static constexpr uint32_t kTmemCols = 512;
@@ -237,30 +246,36 @@ __device__ void producer_role(const FwdParams &p, const Shared &sh, uint32_t sme
 
 // ----------------------------------------------------------------- MMA warp
 
+// S_t = Q_t K_j^T: D/16 MMAs of K = 16.  Q and K tiles are D/64 boxes of
+// [128 rows][64 cols], 128-byte swizzled; step kk reads columns 16kk..16kk+15,
+// i.e. box kk/4 at byte offset 32*(kk%4) inside each 128-byte row.
 template <int D>
 __device__ __forceinline__ void issue_s(uint32_t tmem_s, uint32_t q_tile, uint32_t k_tile) {
     using C = Config<D>;
+    constexpr uint32_t hi = ptx::sdesc_sw128_hi(1024);
+    const uint32_t a0 = ptx::sdesc_sw128_lo(q_tile, 16);
+    const uint32_t b0 = ptx::sdesc_sw128_lo(k_tile, 16);
     #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-        const uint64_t a = ptx::smem_desc_sw128(q_tile + off, 16, 1024);
-        const uint64_t b = ptx::smem_desc_sw128(k_tile + off, 16, 1024);
-        ptx::mma_bf16_ss(tmem_s, a, b, C::kIdescS, kk > 0 ? 1u : 0u);
+        const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+        ptx::mma_bf16_ss(tmem_s, a0 + off, hi, b0 + off, hi, C::kIdescS, kk > 0 ? 1u : 0u);
     }
 }
 
+// O_t (+)= P_t V_j: 8 MMAs of K = 16 keys; P_t is read from TMEM (16 keys =
+// 8 columns of bf16 pairs per step).  V tile: [128 keys][D] as D/64 boxes of
+// [128][64]; the B operand is MN-major (D contiguous): 8-key groups SBO =
+// 1024 B apart, 64-column groups LBO = one box (16 KB) apart.
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_tile,
                                          bool accumulate) {
     using C = Config<D>;
+    constexpr uint32_t hi = ptx::sdesc_sw128_hi(1024);
+    const uint32_t b0 = ptx::sdesc_sw128_lo(v_tile, kChunkBytes);
     #pragma unroll
-    for (int kk = 0; kk < kBC / 16; ++kk) {
-        // V tile: [128 keys][D] as D/64 boxes of [128][64]; the B operand is
-        // MN-major (D contiguous): 8-key groups SBO = 1024 B apart, 64-column
-        // groups LBO = one box (16 KB) apart; 16 keys per MMA step.
-        const uint64_t b = ptx::smem_desc_sw128(v_tile + kk * 16 * 128, kChunkBytes, 1024);
-        ptx::mma_bf16_ts(tmem_o, tmem_p + kk * 8, b, C::kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
-    }
+    for (int kk = 0; kk < kBC / 16; ++kk)
+        ptx::mma_bf16_ts(tmem_o, tmem_p + kk * 8, b0 + ((kk * 16 * 128) >> 4), hi, C::kIdescPV,
+                         (accumulate || kk > 0) ? 1u : 0u);
 }
 
 template <int D>
@@ -342,44 +357,86 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
 }
 
 // ------------------------------------------------------------ softmax warps
+//
+// One softmax warpgroup per Q tile; thread = query row = TMEM lane (warp w
+// reads lanes 32*(w%4)..+31).  Each thread holds its row's 128 scores in
+// registers (the warpgroup runs with 208 registers, see the kernel), so the
+// row maximum is an in-register reduction and many exponentials of
+// independent pairs can be in flight together.
 
-// P for one S tile held in registers (thread = row): p = 2^(c*s - m) for
-// each key, packed to bf16 pairs and written over the first 64 columns of the
-// S tile in TMEM, 32 keys at a time so few packed registers are live.
-// Masked keys already hold -inf*sign(c) and come out as p = 0.
-// Returns the row sum of the fp32 p values.
-__device__ __forceinline__ float exp_pack_store(const uint32_t (&s)[128], float c2, float neg_m,
-                                                uint32_t tP) {
-    float acc0 = 0.f, acc1 = 0.f;
+// Row extreme (max for a positive scale, min for a negative one) of 128 scores.
+__device__ __forceinline__ float row_extreme128(const uint32_t (&s)[128], bool pos) {
+    float a[8];
     #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint32_t pk[16];
+    for (int i = 0; i < 8; ++i) a[i] = __uint_as_float(s[i]);
+    if (pos) {
         #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int c = 32 * q + 2 * i;
-            const float p0 = ptx::ex2(fmaf(__uint_as_float(s[c]), c2, neg_m));
-            const float p1 = ptx::ex2(fmaf(__uint_as_float(s[c + 1]), c2, neg_m));
-            acc0 += p0;
-            acc1 += p1;
-            pk[i] = ptx::pack_bf16x2(p0, p1);
-        }
-        ptx::tmem_store_16cols(tP + 16 * q, pk);
+        for (int c = 8; c < 120; c += 16)
+            #pragma unroll
+            for (int i = 0; i < 8; ++i)
+                a[i] = ptx::max3(a[i], __uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1]));
+        #pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = ptx::max3(a[i], __uint_as_float(s[120 + 2 * i]), __uint_as_float(s[121 + 2 * i]));
+        return fmaxf(ptx::max3(a[0], a[1], a[2]), ptx::max3(a[3], ptx::max3(a[4], a[5], a[6]), a[7]));
     }
-    return acc0 + acc1;
+    #pragma unroll
+    for (int c = 8; c < 120; c += 16)
+        #pragma unroll
+        for (int i = 0; i < 8; ++i)
+            a[i] = ptx::min3(a[i], __uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1]));
+    #pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = ptx::min3(a[i], __uint_as_float(s[120 + 2 * i]), __uint_as_float(s[121 + 2 * i]));
+    return fminf(ptx::min3(a[0], a[1], a[2]), ptx::min3(a[3], ptx::min3(a[4], a[5], a[6]), a[7]));
+}
+
+// P for the row's 128 scores: p = 2^(c*s - m), packed to bf16 pairs (round
+// to nearest even) and stored over the first 64 TMEM columns of the S tile.
+// Row sums: of the fp32 p (for LSE) and of the bf16 p that P V actually
+// uses, which normalises O: the weights then sum to one exactly, so a
+// dominant key carries no rounding error into O.  Masked keys hold
+// -inf*sign(c) and come out as p = 0.
+__device__ __forceinline__ void exp_pack_store128(const uint32_t (&s)[128], float c2, float neg_m, uint32_t tP,
+                                                  float &sum_exact, float &sum_rounded) {
+    const uint64_t c2x2 = ptx::f2_pack(c2, c2), mx2 = ptx::f2_pack(neg_m, neg_m);
+    uint64_t acc_e[4];
+    #pragma unroll
+    for (int i = 0; i < 4; ++i) acc_e[i] = ptx::f2_pack(0.f, 0.f);
+    float r[8];
+    #pragma unroll
+    for (int i = 0; i < 8; ++i) r[i] = 0.f;
+    uint32_t pk[64];
+    #pragma unroll
+    for (int i = 0; i < 64; ++i) {
+        const uint64_t t = ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
+                                       c2x2, mx2);
+        float t0, t1;
+        ptx::f2_unpack(t, t0, t1);
+        const float p0 = ptx::ex2(t0), p1 = ptx::ex2(t1);
+        acc_e[i & 3] = ptx::f2_add(acc_e[i & 3], ptx::f2_pack(p0, p1));
+        pk[i] = ptx::pack_bf16x2(p0, p1);
+        ptx::add_bf16x2_to_f32(r[2 * (i & 3)], r[2 * (i & 3) + 1], pk[i]);
+    }
+    #pragma unroll
+    for (int q = 0; q < 4; ++q)
+        ptx::tmem_store_16cols(tP + 16 * q, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * q]));
+    float e0, e1;
+    ptx::f2_unpack(ptx::f2_add(ptx::f2_add(acc_e[0], acc_e[1]), ptx::f2_add(acc_e[2], acc_e[3])), e0, e1);
+    sum_exact = e0 + e1;
+    sum_rounded = ((r[0] + r[1]) + (r[2] + r[3])) + ((r[4] + r[5]) + (r[6] + r[7]));
 }
 
 template <int D>
-__device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem, int tile,
-                             int quad, int lane) {
+__device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem, int tile, int quad, int lane) {
     const int row = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tS = tmem + lane_off + tile * 128;
     const uint32_t tO = tmem + lane_off + 256 + tile * D;
     const float c2 = p.c2;
+    const bool pos = c2 > 0.f;
     // A masked key must never win the row extreme and must give p = 0:
     // -inf for a positive scale, +inf for a negative one (the host never
     // passes c2 == 0, see fa_fwd).
-    const float mask_val = c2 > 0.f ? -INFINITY : INFINITY;
+    const float mask_val = pos ? -INFINITY : INFINITY;
     uint32_t s_phase = 0, o_phase = 0;
 
     for (int k = 0;; ++k) {
@@ -391,7 +448,8 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
         const int qg = item.q0 + tile * kBR + row;   // this thread's query row
         const int key_lim = p.causal ? min(p.Nk, qg + 1) : p.Nk;
         float m_ref = -INFINITY;   // log2-domain reference maximum
-        float l = 0.f;
+        float l = 0.f;             // sum of p (fp32), for LSE
+        float l_rounded = 0.f;     // sum of the bf16 p that P V uses, for O
 
         for (int j = 0; j < nk; ++j) {
             if (!wait_bar(sh.s_full0 + 8 * tile, s_phase, sh.abort_flag, 2 + tile, w, j)) return;
@@ -399,32 +457,13 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
             ptx::tc_fence_after_sync();
             uint32_t s[128];
             ptx::tmem_load_128cols(tS, s);
-
             const int kvalid = key_lim - j * kBC;
-            const bool masked = __any_sync(0xffffffffu, kvalid < kBC);   // warp-uniform path
-            if (masked) {
+            if (__any_sync(0xffffffffu, kvalid < kBC)) {   // warp-uniform masked path
                 #pragma unroll
                 for (int c = 0; c < 128; ++c)
                     if (c >= kvalid) s[c] = __float_as_uint(mask_val);
             }
-            float mx;
-            if (c2 > 0.f) {
-                float a = __uint_as_float(s[0]), b = __uint_as_float(s[1]);
-                #pragma unroll
-                for (int c = 2; c < 128; c += 2) {
-                    a = fmaxf(a, __uint_as_float(s[c]));
-                    b = fmaxf(b, __uint_as_float(s[c + 1]));
-                }
-                mx = fmaxf(a, b);
-            } else {
-                float a = __uint_as_float(s[0]), b = __uint_as_float(s[1]);
-                #pragma unroll
-                for (int c = 2; c < 128; c += 2) {
-                    a = fminf(a, __uint_as_float(s[c]));
-                    b = fminf(b, __uint_as_float(s[c + 1]));
-                }
-                mx = fminf(a, b);
-            }
+            const float mx = row_extreme128(s, pos);
             const float m_tile = kvalid > 0 ? mx * c2 : -INFINITY;
             float alpha = 1.f;
             if (m_tile > m_ref + kTau) {
@@ -432,10 +471,14 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
                 m_ref = m_tile;
             }
             l *= alpha;
+            l_rounded *= alpha;
 
             // m_ref is finite once a row has seen a key (every row sees key 0
             // in its first tile); the guard keeps a fully masked row at p = 0.
-            l += exp_pack_store(s, c2, m_ref == -INFINITY ? 0.f : -m_ref, tS);
+            float se, sr;
+            exp_pack_store128(s, c2, m_ref == -INFINITY ? 0.f : -m_ref, tS, se, sr);
+            l += se;
+            l_rounded += sr;
             // Rescale O_t in TMEM when this warp's reference maximum moved
             // (PV_t(j-1) has completed, see the header; PV_t(j) waits for us).
             if (__any_sync(0xffffffffu, j > 0 && alpha != 1.f)) {
@@ -457,7 +500,7 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
         if (!wait_bar(sh.o_full0 + 8 * tile, o_phase, sh.abort_flag, 2 + tile, w, nk)) return;
         o_phase ^= 1u;
         ptx::tc_fence_after_sync();
-        const float inv_l = 1.f / l;
+        const float inv_l = 1.f / l_rounded;
         const bool live = qg < p.Nq;
         __nv_bfloat16 *orow = p.O + (static_cast<size_t>(item.bh) * p.Nq + qg) * D;
         #pragma unroll 1
@@ -467,16 +510,14 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
             uint32_t h[16];
             #pragma unroll
             for (int i = 0; i < 16; ++i)
-                h[i] = ptx::pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
-                                        __uint_as_float(o[2 * i + 1]) * inv_l);
+                h[i] = ptx::pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
             if (live) {
                 uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
                 #pragma unroll
                 for (int i = 0; i < 4; ++i) dst[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
             }
         }
-        if (live)
-            p.LSE[static_cast<size_t>(item.bh) * p.Nq + qg] = (m_ref + ptx::lg2(l)) * 0.69314718055994531f;
+        if (live) p.LSE[static_cast<size_t>(item.bh) * p.Nq + qg] = (m_ref + ptx::lg2(l)) * 0.69314718055994531f;
         ptx::tc_fence_before_sync();
     }
 }
@@ -494,8 +535,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     const uint32_t smem_q = base;
     const uint32_t smem_ring = base + C::kQBytes;
     const uint32_t bars = base + C::kBarOffset;
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(base_ptr + C::kBarOffset + 200);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(base_ptr + C::kBarOffset + 208);
+    // barrier block: 9 fixed barriers, 2 * kSlots ring barriers, then the
+    // TMEM address holder and the abort flag
+    constexpr int kHolder = 72 + 16 * C::kSlots;
+    static_assert(kHolder + 8 <= 256, "barrier block overflows its 256 bytes");
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(base_ptr + C::kBarOffset + kHolder);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base_ptr + C::kBarOffset + kHolder + 4);
 
     Shared sh;
     sh.q_full = bars + 0;
@@ -542,9 +587,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     const uint32_t tmem = *tmem_holder;
 
     uint32_t loads_issued = 0, q_arms = 0;
-    if (warp < 8) {
+    if (warp < kSoftmaxWarps) {
+        ptx::setmaxnreg_inc<kSoftmaxRegs>();
         softmax_role<D>(p, sh, tmem, warp >> 2, warp & 3, lane);
     } else if (warp == kProducerWarp) {
+        ptx::setmaxnreg_dec<kOtherRegs>();
         if (lane == 0) {
             producer_role<D>(p, sh, smem_q, smem_ring, loads_issued, q_arms);
             // Drain: every copy this CTA started must land before it exits.
@@ -555,7 +602,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         }
         __syncwarp();
     } else {
-        if (lane == 0) mma_role<D>(p, sh, tmem, smem_q, smem_ring);
+        ptx::setmaxnreg_dec<kOtherRegs>();
+        if (warp == kMmaWarp && lane == 0) mma_role<D>(p, sh, tmem, smem_q, smem_ring);
         __syncwarp();
     }
 
