@@ -88,6 +88,43 @@ void plan_schedule(fa::FwdParams &p, int grid_ctas) {
     p.n_items = static_cast<int>(NP + split);
 }
 
+// Heads per group of the item order.  Non-causal items all cost the same,
+// so heads are grouped to keep their K and V within 48 MB (well inside the
+// 126 MB L2, leaving room for the streamed Q and O).  Causal items differ in
+// cost; one group over all heads keeps the list heaviest-first, which the
+// snake assignment needs to balance the CTAs.
+int heads_per_group(int64_t BH, int64_t Nk, int d, int causal) {
+    if (causal) return static_cast<int>(BH);
+    const int64_t kv_bytes = Nk * d * 2 * 2;
+    int64_t hg = (int64_t{48} << 20) / (kv_bytes > 0 ? kv_bytes : 1);
+    if (hg < 1) hg = 1;
+    if (hg > BH) hg = BH;
+    return static_cast<int>(hg);
+}
+
+// Shapes, scale and schedule of one call (everything but pointers and maps);
+// returns the grid size.
+int setup_params(fa::FwdParams &p, int B, int H, int Nq, int Nk, int d, float scale, int causal, int sms) {
+    std::memset(&p, 0, sizeof p);
+    const int64_t BH = static_cast<int64_t>(B) * H;
+    p.BH = static_cast<int>(BH);
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.Tr = (Nq + fa::kBR - 1) / fa::kBR;
+    p.Tc = (Nk + fa::kBC - 1) / fa::kBC;
+    p.P = (p.Tr + 1) / 2;
+    p.causal = causal != 0;
+    // c2 = scale * log2(e).  A zero scale is run as the smallest normal float:
+    // every score then changes by at most |S| * 2^-126, far below fp32
+    // resolution of the outputs, and masked keys keep an exact p = 0.
+    double c2 = static_cast<double>(scale) * 1.4426950408889634;
+    if (scale == 0.0f) c2 = 1.1754943508222875e-38 * 1.4426950408889634;
+    p.c2 = static_cast<float>(c2);
+    p.heads_per_group = heads_per_group(BH, Nk, d, causal);
+    plan_schedule(p, sms);
+    return p.n_items < sms ? p.n_items : sms;
+}
+
 struct DeviceInfo {
     int sms = 0;
     bool attr64 = false, attr128 = false;
@@ -130,31 +167,41 @@ extern "C" fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O
     }
 
     fa::FwdParams p;
-    std::memset(&p, 0, sizeof p);
+    const int grid = setup_params(p, B, H, Nq, Nk, d, scale, causal, sms);
     const int64_t BH = static_cast<int64_t>(B) * H;
     if (!make_map(&p.tmQ, Q, BH, Nq, d) || !make_map(&p.tmK, K, BH, Nk, d) || !make_map(&p.tmV, V, BH, Nk, d))
         return FA_ERR_CUDA;
     p.O = static_cast<__nv_bfloat16 *>(O);
     p.LSE = LSE;
-    p.BH = static_cast<int>(BH);
-    p.Nq = Nq;
-    p.Nk = Nk;
-    p.Tr = (Nq + fa::kBR - 1) / fa::kBR;
-    p.Tc = (Nk + fa::kBC - 1) / fa::kBC;
-    p.P = (p.Tr + 1) / 2;
-    p.causal = causal != 0;
-    // c2 = scale * log2(e).  A zero scale is run as the smallest normal float:
-    // every score then changes by at most |S| * 2^-126, far below fp32
-    // resolution of the outputs, and masked keys keep an exact p = 0.
-    double c2 = static_cast<double>(scale) * 1.4426950408889634;
-    if (scale == 0.0f) c2 = 1.1754943508222875e-38 * 1.4426950408889634;
-    p.c2 = static_cast<float>(c2);
-    plan_schedule(p, sms);
-    const int grid = p.n_items < sms ? p.n_items : sms;
 
     std::lock_guard<std::mutex> lock(g_dev_mu);
     return d == 64 ? launch<64>(p, grid, reinterpret_cast<cudaStream_t>(stream), *attr_done)
                    : launch<128>(p, grid, reinterpret_cast<cudaStream_t>(stream), *attr_done);
+}
+
+extern "C" fa_status fa_schedule(int B, int H, int Nq, int Nk, int d, int causal, int num_sms, int32_t *items,
+                                 int64_t capacity, int64_t *n_items) {
+    if (!n_items || num_sms < 1) return FA_ERR_INVALID_ARG;
+    const float scale = 1.0f;
+    char dummy[16] __attribute__((aligned(16)));
+    fa_status st = validate(dummy, dummy, dummy, dummy, reinterpret_cast<float *>(dummy), B, H, Nq, Nk, d, scale);
+    if (st != FA_OK) return st;
+    fa::FwdParams p;
+    const int grid = setup_params(p, B, H, Nq, Nk, d, scale, causal, num_sms);
+    *n_items = p.n_items;
+    if (!items) return FA_OK;
+    if (capacity < p.n_items) return FA_ERR_INVALID_ARG;
+    int64_t n = 0;
+    for (int b = 0; b < grid; ++b) {
+        for (int k = 0;; ++k) {
+            const int w = fa::item_of_round(p, k, b, grid);
+            if (w < 0) break;
+            const fa::Item it = fa::decode_item(p, w);
+            int32_t *out = items + 6 * n++;
+            out[0] = b; out[1] = k; out[2] = it.bh; out[3] = it.q0; out[4] = it.nk[0]; out[5] = it.ntiles > 1 ? it.nk[1] : 0;
+        }
+    }
+    return n == p.n_items ? FA_OK : FA_ERR_INVALID_ARG;
 }
 
 extern "C" fa_status fa_fwd_host(const void *hQ, const void *hK, const void *hV, void *hO, float *hLSE,

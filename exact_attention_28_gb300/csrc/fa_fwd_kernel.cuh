@@ -14,7 +14,8 @@
 // Q tile for load balancing at the end of the list.  CTAs are persistent: the
 // grid is at most one CTA per SM and each CTA walks the item list with a
 // static stride, reversing direction every round ("snake") so heavy and light
-// items (causal) even out.  Items are ordered heaviest first.
+// items (causal) even out.  Items come in groups of heads whose K/V fit in
+// L2 together, heaviest first inside a group.
 //
 // Roles inside a CTA (384 threads, 3 warpgroups):
 //   warps 0-3   softmax for Q tile 0 (TMEM lanes 0-127: thread = query row)
@@ -101,6 +102,7 @@ struct FwdParams {
     int P;             // Q-tile pairs per head = ceil(Tr / 2)
     int n_pair_items;  // items [0, n_pair_items) are whole pairs
     int n_items;       // the rest are single tiles of the last pairs in order
+    int heads_per_group;  // items are ordered by groups of heads (L2 locality)
     int causal;
     float c2;          // scale * log2(e)
 };
@@ -112,9 +114,11 @@ struct Item {
     int nk[2];     // K/V tiles visited by each tile (0 if absent)
 };
 
-// Item w of the list: pairs ordered by descending pair index (for causal the
-// heaviest first), heads inner; the lightest pairs are split into singles.
-__device__ __forceinline__ Item decode_item(const FwdParams &p, int w) {
+// Item w of the list.  Heads are taken in groups of heads_per_group whose
+// K/V fit in L2 together; inside a group, pairs go by descending pair index
+// (for causal the heaviest first), heads inner.  The last pairs of the list
+// (the lightest) are split into single-tile items.
+__host__ __device__ __forceinline__ Item decode_item(const FwdParams &p, int w) {
     int r, first, single;
     if (w < p.n_pair_items) {
         r = w; first = 0; single = 0;
@@ -122,9 +126,14 @@ __device__ __forceinline__ Item decode_item(const FwdParams &p, int w) {
         const int s = w - p.n_pair_items;
         r = p.n_pair_items + (s >> 1); first = s & 1; single = 1;
     }
-    const int pair = p.P - 1 - r / p.BH;
+    const int per_group = p.heads_per_group * p.P;
+    const int g = r / per_group;
+    const int rr = r - g * per_group;
+    const int rest = p.BH - g * p.heads_per_group;
+    const int gsize = p.heads_per_group < rest ? p.heads_per_group : rest;
+    const int pair = p.P - 1 - rr / gsize;
     Item it;
-    it.bh = r % p.BH;
+    it.bh = g * p.heads_per_group + rr % gsize;
     it.q0 = (2 * pair + first) * kBR;
     const int left = p.Tr - (2 * pair + first);
     it.ntiles = single ? 1 : (left >= 2 ? 2 : 1);
@@ -134,8 +143,10 @@ __device__ __forceinline__ Item decode_item(const FwdParams &p, int w) {
         if (t < it.ntiles) {
             nk = p.Tc;
             if (p.causal) {
-                const int q_end = min(p.Nq, it.q0 + (t + 1) * kBR);  // rows >= Nq are padding
-                nk = min(p.Tc, (q_end - 1) / kBC + 1);
+                const int q_end_raw = it.q0 + (t + 1) * kBR;
+                const int q_end = q_end_raw < p.Nq ? q_end_raw : p.Nq;   // rows >= Nq are padding
+                const int need = (q_end - 1) / kBC + 1;
+                nk = need < p.Tc ? need : p.Tc;
             }
         }
         it.nk[t] = nk;
@@ -143,12 +154,13 @@ __device__ __forceinline__ Item decode_item(const FwdParams &p, int w) {
     return it;
 }
 
-// Item index of round k for this CTA (snake order), or -1 when done.
-__device__ __forceinline__ int item_of_round(const FwdParams &p, int k) {
-    const int G = gridDim.x;
-    const int b = blockIdx.x;
+// Item index of round k for CTA b of G (snake order), or -1 when done.
+__host__ __device__ __forceinline__ int item_of_round(const FwdParams &p, int k, int b, int G) {
     const int w = k * G + ((k & 1) ? (G - 1 - b) : b);
     return w < p.n_items ? w : -1;
+}
+__device__ __forceinline__ int item_of_round(const FwdParams &p, int k) {
+    return item_of_round(p, k, blockIdx.x, gridDim.x);
 }
 
 struct Shared {
@@ -512,9 +524,10 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
             for (int i = 0; i < 16; ++i)
                 h[i] = ptx::pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
             if (live) {
+                // streaming stores: O is written once, keep L2 for K/V
                 uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
                 #pragma unroll
-                for (int i = 0; i < 4; ++i) dst[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+                for (int i = 0; i < 4; ++i) __stcs(dst + i, make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]));
             }
         }
         if (live) p.LSE[static_cast<size_t>(item.bh) * p.Nq + qg] = (m_ref + ptx::lg2(l)) * 0.69314718055994531f;

@@ -41,6 +41,8 @@ def load_library(path: str | None = None):
     lib.fa_fwd_host.restype = i
     lib.fa_check_device_status.argtypes = [vp]
     lib.fa_check_device_status.restype = i
+    lib.fa_schedule.argtypes = [i, i, i, i, i, i, i, vp, ctypes.c_int64, vp]
+    lib.fa_schedule.restype = i
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
     if path == LIB_PATH:
@@ -104,6 +106,18 @@ def fa_fwd_host(hq, hk, hv, ho, hlse, dq, dk, dv, do, dlse, scale, causal=False,
 def check_device_status(stream=None):
     """Synchronise and raise if a kernel of the library hit a wait limit."""
     _check(load_library().fa_check_device_status(_stream_handle(stream)))
+
+
+def schedule(B, H, Nq, Nk, d, causal, num_sms):
+    """The kernel's work list: int32 array [n_items, 6] of
+    (cta, round, batch*head, first query row, KV tiles of tile 0, of tile 1)."""
+    import numpy as np
+    lib = load_library()
+    n = ctypes.c_int64(0)
+    _check(lib.fa_schedule(B, H, Nq, Nk, d, int(bool(causal)), num_sms, None, 0, ctypes.byref(n)))
+    out = np.zeros((n.value, 6), dtype=np.int32)
+    _check(lib.fa_schedule(B, H, Nq, Nk, d, int(bool(causal)), num_sms, out.ctypes.data, n.value, ctypes.byref(n)))
+    return out
 
 
 def raw_fa_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Nq, Nk, d, scale, causal, stream_handle=0) -> int:

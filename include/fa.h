@@ -91,6 +91,24 @@ fa_status fa_fwd_host(const void *hQ, const void *hK, const void *hV, void *hO, 
  */
 fa_status fa_check_device_status(fa_stream_t stream);
 
+/*
+ * fa_schedule -- the work list fa_fwd would run for these shapes on a GPU
+ * with num_sms SMs (host only; no GPU needed).  The kernel's persistent CTAs
+ * each walk this list; a work item is one (batch*head, pair of 128-row query
+ * tiles) or a single tile, in the order "9.4 FlashAttention 与 FlashMLA"
+ * section 9.4.4 describes for FA2: parallel over batch x heads x query
+ * blocks, each block looping over all key/value blocks it can see.
+ *
+ *   items     int32 [capacity][6], caller-owned, may be NULL to only count:
+ *             {cta, round, batch*head, first query row, KV tiles of query tile 0,
+ *              KV tiles of query tile 1 (0 if the item holds one tile)}
+ *   n_items   out: number of items
+ * Returns FA_ERR_INVALID_ARG for bad sizes or capacity < *n_items (after
+ * setting *n_items), FA_ERR_UNSUPPORTED for d not in {64, 128}.
+ */
+fa_status fa_schedule(int B, int H, int Nq, int Nk, int d, int causal, int num_sms, int32_t *items,
+                      int64_t capacity, int64_t *n_items);
+
 /* A static, human-readable name for a status code (never NULL). */
 const char *fa_status_string(fa_status s);
 

@@ -1,0 +1,84 @@
+"""The persistent kernel's work list, enumerated on the host (no GPU).
+
+Every (batch*head, 128-row query tile) must be computed exactly once, each
+with the key/value tiles its rows can see (all of them, or those up to the
+diagonal under the causal mask), and the rounds must balance across CTAs.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import __graft_entry__  # noqa: F401
+from exact_attention_28_gb300 import build, ops
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    build.build()
+    ops.load_library()
+
+
+def expand(items):
+    """(cta, round, bh, q0, nk0, nk1) -> list of (bh, q_start, nk)."""
+    tiles = []
+    for cta, rnd, bh, q0, nk0, nk1 in items.tolist():
+        tiles.append((bh, q0, nk0))
+        if nk1 > 0:
+            tiles.append((bh, q0 + 128, nk1))
+    return tiles
+
+
+SHAPES = [
+    (1, 1, 256, 256, 64, False), (4, 16, 1024, 1024, 64, True), (2, 16, 4096, 4096, 128, False),
+    (1, 32, 16384, 16384, 128, True), (8, 32, 128, 8192, 128, False), (8, 32, 128, 8229, 128, False),
+    (1, 3, 300, 1000, 64, True), (1, 3, 1000, 300, 128, True), (2, 5, 129, 129, 64, False), (1, 1, 1, 1, 64, True),
+    (3, 7, 640, 129, 128, True), (8, 64, 200, 160, 64, True),
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,causal", SHAPES)
+@pytest.mark.parametrize("sms", [1, 7, 148, 152])
+def test_every_tile_exactly_once_with_its_kv_range(B, H, Nq, Nk, d, causal, sms):
+    items = ops.schedule(B, H, Nq, Nk, d, causal, sms)
+    tiles = expand(items)
+    Tr, Tc = math.ceil(Nq / 128), math.ceil(Nk / 128)
+    assert len(tiles) == B * H * Tr
+    assert len(set((bh, q) for bh, q, _ in tiles)) == B * H * Tr
+    for bh, q, nk in tiles:
+        assert 0 <= bh < B * H and q % 128 == 0 and q < Nq
+        want = min(Tc, (min(Nq, q + 128) - 1) // 128 + 1) if causal else Tc
+        assert nk == want, (bh, q, nk, want)
+    # each CTA walks consecutive rounds 0, 1, 2, ...
+    for cta in np.unique(items[:, 0]):
+        rounds = np.sort(items[items[:, 0] == cta, 1])
+        assert np.array_equal(rounds, np.arange(len(rounds)))
+    assert items[:, 0].max() < sms
+
+
+def cta_loads(items, key=lambda nk: 1):
+    load = {}
+    for cta, _, _, _, nk0, nk1 in items.tolist():
+        load[cta] = load.get(cta, 0) + key(nk0) + (key(nk1) if nk1 else 0)
+    return np.array(list(load.values()), dtype=np.float64)
+
+
+def test_noncausal_rounds_fill_the_machine():
+    # 1024 query tiles on 152 SMs: no CTA gets more than ceil(1024/152) = 7 tiles
+    items = ops.schedule(2, 16, 4096, 4096, 128, False, 152)
+    assert cta_loads(items).max() == 7
+
+
+def test_causal_load_balance():
+    # the long causal workload: KV-tile work per CTA within 10% of the mean
+    items = ops.schedule(1, 32, 16384, 16384, 128, True, 152)
+    load = cta_loads(items, key=lambda nk: nk)
+    assert load.max() / load.mean() < 1.10
+
+
+def test_schedule_argument_errors():
+    n = ops.ctypes.c_int64(0)
+    lib = ops.load_library()
+    assert lib.fa_schedule(1, 1, 128, 128, 96, 0, 152, None, 0, ops.ctypes.byref(n)) == ops.FA_ERR_UNSUPPORTED
+    assert lib.fa_schedule(0, 1, 128, 128, 64, 0, 152, None, 0, ops.ctypes.byref(n)) == ops.FA_ERR_INVALID_ARG
+    assert lib.fa_schedule(1, 1, 128, 128, 64, 0, 0, None, 0, ops.ctypes.byref(n)) == ops.FA_ERR_INVALID_ARG
