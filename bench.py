@@ -78,6 +78,32 @@ def profiled_traffic():
         return None
 
 
+def reduce_max(values, world, device="cuda"):
+    """Element-wise maximum of a list of floats over all ranks (the timing of
+    a multi-GPU run is its slowest rank)."""
+    if world <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def aggregate_tflops(flops_per_rank, ms_per_step_max, world):
+    """Whole-job throughput: every rank's work over the slowest rank's time."""
+    return world * flops_per_rank / (ms_per_step_max * 1e-3) / 1e12
+
+
+def shard_heads(num_heads, rank, world):
+    """Contiguous [start, stop) slice of the B*H independent heads for one rank
+    (heads are independent problems, so a strong-scaling split needs no
+    communication on the data path)."""
+    base, extra = divmod(num_heads, world)
+    start = rank * base + min(rank, extra)
+    return start, start + base + (1 if rank < extra else 0)
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json"), encoding="utf-8") as fh:
@@ -281,10 +307,7 @@ def run_ours(args, w):
     ops.check_device_status()
     total_ms = starts[0].elapsed_time(ends[-1])
     launch_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
-    if world > 1:
-        red = torch.tensor([total_ms, launch_ms], device="cuda")
-        dist.all_reduce(red, op=dist.ReduceOp.MAX)
-        total_ms, launch_ms = red.tolist()
+    total_ms, launch_ms = reduce_max([total_ms, launch_ms], world)
     if sampler:
         time.sleep(0.25)
         sampler.stop()
@@ -293,14 +316,12 @@ def run_ours(args, w):
     e2e_ms = float("nan")
     if not args.no_e2e:
         e2e_ms = run_e2e(args, w, hq, hk, hv, sets[0], scale, stream)
-    if world > 1 and not args.no_e2e:
-        red = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(red, op=dist.ReduceOp.MAX)
-        e2e_ms = red.item()
+    if not args.no_e2e:
+        e2e_ms = reduce_max([e2e_ms], world)[0]
     if rank == 0:
         peaks, peak_src = measured_peaks()
         ms_per_step = total_ms / args.steps
-        value = world * w.flops / (ms_per_step * 1e-3) / 1e12
+        value = aggregate_tflops(w.flops, ms_per_step, world)
         achieved = w.flops / (launch_ms * 1e-3) / 1e12
         peak = float(peaks["bf16_tflops"])
         traffic = profiled_traffic()
@@ -315,7 +336,7 @@ def run_ours(args, w):
                          "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
                          "kernel": "fa_fwd_kernel<%d>" % w.d, "launch_ms": launch_ms},
             "e2e": None if args.no_e2e else {
-                "value": world * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+                "value": aggregate_tflops(w.flops, e2e_ms, world), "unit": "TFLOPS",
                 "h2d_bytes_per_step": 2 * (hq.numel() + 2 * hk.numel()),
                 "d2h_bytes_per_step": 2 * hq.numel() + 4 * w.B * w.H * w.Nq,
                 "ms_per_step": e2e_ms},
