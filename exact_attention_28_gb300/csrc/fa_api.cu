@@ -103,8 +103,10 @@ int heads_per_group(int64_t BH, int64_t Nk, int d, int causal) {
 }
 
 // Shapes, scale and schedule of one call (everything but pointers and maps);
-// returns the grid size.
-int setup_params(fa::FwdParams &p, int B, int H, int Nq, int Nk, int d, float scale, int causal, int sms) {
+// returns the grid size.  kv_splits > 1 cuts every item's key range into that
+// many slices, each a work item of its own.
+int setup_params(fa::FwdParams &p, int B, int H, int Nq, int Nk, int d, float scale, int causal, int sms,
+                 int kv_splits = 1) {
     std::memset(&p, 0, sizeof p);
     const int64_t BH = static_cast<int64_t>(B) * H;
     p.BH = static_cast<int>(BH);
@@ -121,8 +123,38 @@ int setup_params(fa::FwdParams &p, int B, int H, int Nq, int Nk, int d, float sc
     if (scale == 0.0f) c2 = 1.1754943508222875e-38 * 1.4426950408889634;
     p.c2 = static_cast<float>(c2);
     p.heads_per_group = heads_per_group(BH, Nk, d, causal);
-    plan_schedule(p, sms);
+    p.kv_splits = kv_splits > 1 ? kv_splits : 1;
+    if (p.kv_splits > 1) {
+        const int64_t NP = static_cast<int64_t>(p.BH) * p.P;
+        p.n_pair_items = static_cast<int>(NP);
+        p.n_items = static_cast<int>(NP * p.kv_splits);
+    } else {
+        plan_schedule(p, sms);
+    }
     return p.n_items < sms ? p.n_items : sms;
+}
+
+// Key-range slices for the split path.  Splitting costs a partial write, a
+// merge and a re-read per slice, so it pays only when the unsplit work list
+// leaves most SMs idle (at most half of them busy); then enough slices to
+// give every SM about one item, never more slices than K/V tiles, at most 64.
+int choose_splits(int64_t BH, int Nq, int Nk, int sms) {
+    const int64_t pairs = BH * ((Nq + 2 * fa::kBR - 1) / (2 * fa::kBR));
+    if (2 * pairs > sms) return 1;
+    const int64_t tc = (Nk + fa::kBC - 1) / fa::kBC;
+    int64_t s = (static_cast<int64_t>(sms) + pairs - 1) / pairs;
+    if (s > tc) s = tc;
+    if (s > 64) s = 64;
+    return s < 1 ? 1 : static_cast<int>(s);
+}
+
+// Workspace of the split path: [splits][BH][Nq][d] fp32 partial outputs, then
+// [splits][BH][Nq] fp32 partial LSE at a 256-byte boundary.
+size_t splitkv_o_bytes(int64_t BH, int Nq, int d, int splits) {
+    return ((static_cast<size_t>(splits) * BH * Nq * d * 4) + 255) & ~static_cast<size_t>(255);
+}
+size_t splitkv_bytes(int64_t BH, int Nq, int d, int splits) {
+    return splitkv_o_bytes(BH, Nq, d, splits) + static_cast<size_t>(splits) * BH * Nq * 4;
 }
 
 struct DeviceInfo {
@@ -147,47 +179,112 @@ fa_status launch(const fa::FwdParams &p, int grid, cudaStream_t stream, bool &at
 
 }  // namespace
 
-extern "C" fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
-                            int Nq, int Nk, int d, float scale, int causal, fa_stream_t stream) {
-    fa_status st = validate(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale);
-    if (st != FA_OK) return st;
+namespace {
 
+fa_status device_info(int d, int &sms, bool *&attr_done) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DeviceInfo &info = g_dev[dev];
+    if (info.sms == 0 && cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return FA_ERR_CUDA;
+    sms = info.sms;
+    attr_done = d == 64 ? &info.attr64 : &info.attr128;
+    return FA_OK;
+}
+
+// Encodes the maps and launches the attention kernel (partials when
+// kv_splits > 1, into O_part / LSE_part).
+fa_status run_forward(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int Nq,
+                      int Nk, int d, float scale, int causal, int kv_splits, float *O_part, float *LSE_part,
+                      cudaStream_t stream) {
     int sms;
     bool *attr_done;
-    {
-        std::lock_guard<std::mutex> lock(g_dev_mu);
-        DeviceInfo &info = g_dev[dev];
-        if (info.sms == 0 &&
-            cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return FA_ERR_CUDA;
-        sms = info.sms;
-        attr_done = d == 64 ? &info.attr64 : &info.attr128;
-    }
-
+    fa_status st = device_info(d, sms, attr_done);
+    if (st != FA_OK) return st;
     fa::FwdParams p;
-    const int grid = setup_params(p, B, H, Nq, Nk, d, scale, causal, sms);
+    const int grid = setup_params(p, B, H, Nq, Nk, d, scale, causal, sms, kv_splits);
     const int64_t BH = static_cast<int64_t>(B) * H;
     if (!make_map(&p.tmQ, Q, BH, Nq, d) || !make_map(&p.tmK, K, BH, Nk, d) || !make_map(&p.tmV, V, BH, Nk, d))
         return FA_ERR_CUDA;
     p.O = static_cast<__nv_bfloat16 *>(O);
     p.LSE = LSE;
-
+    p.O_part = O_part;
+    p.LSE_part = LSE_part;
     std::lock_guard<std::mutex> lock(g_dev_mu);
-    return d == 64 ? launch<64>(p, grid, reinterpret_cast<cudaStream_t>(stream), *attr_done)
-                   : launch<128>(p, grid, reinterpret_cast<cudaStream_t>(stream), *attr_done);
+    return d == 64 ? launch<64>(p, grid, stream, *attr_done) : launch<128>(p, grid, stream, *attr_done);
 }
 
-extern "C" fa_status fa_schedule(int B, int H, int Nq, int Nk, int d, int causal, int num_sms, int32_t *items,
-                                 int64_t capacity, int64_t *n_items) {
-    if (!n_items || num_sms < 1) return FA_ERR_INVALID_ARG;
+fa_status run_merge(const float *O_part, const float *LSE_part, void *O, float *LSE, int64_t rows, int d, int splits,
+                    cudaStream_t stream) {
+    const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
+    if (d == 64)
+        fa::fa_merge_kernel<64><<<blocks, 256, 0, stream>>>(O_part, LSE_part, static_cast<__nv_bfloat16 *>(O), LSE,
+                                                           rows, splits);
+    else
+        fa::fa_merge_kernel<128><<<blocks, 256, 0, stream>>>(O_part, LSE_part, static_cast<__nv_bfloat16 *>(O), LSE,
+                                                            rows, splits);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                            int Nq, int Nk, int d, float scale, int causal, fa_stream_t stream) {
+    fa_status st = validate(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale);
+    if (st != FA_OK) return st;
+    return run_forward(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, causal, 1, nullptr, nullptr,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" fa_status fa_splitkv_workspace(int B, int H, int Nq, int Nk, int d, int causal, int *num_splits,
+                                          size_t *bytes) {
+    (void)causal;
+    if (!num_splits || !bytes || *num_splits < 0) return FA_ERR_INVALID_ARG;
+    char dummy[16] __attribute__((aligned(16)));
+    fa_status st = validate(dummy, dummy, dummy, dummy, reinterpret_cast<float *>(dummy), B, H, Nq, Nk, d, 1.0f);
+    if (st != FA_OK) return st;
+    const int64_t BH = static_cast<int64_t>(B) * H;
+    if (*num_splits == 0) {
+        int sms;
+        bool *attr_done;
+        st = device_info(d, sms, attr_done);
+        if (st != FA_OK) return st;
+        *num_splits = choose_splits(BH, Nq, Nk, sms);
+    }
+    if (*num_splits > 256) return FA_ERR_INVALID_ARG;
+    *bytes = splitkv_bytes(BH, Nq, d, *num_splits);
+    return FA_OK;
+}
+
+extern "C" fa_status fa_fwd_splitkv(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                                    int Nq, int Nk, int d, float scale, int causal, int num_splits,
+                                    void *workspace, size_t workspace_bytes, fa_stream_t stream) {
+    fa_status st = validate(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale);
+    if (st != FA_OK) return st;
+    if (num_splits < 1 || num_splits > 256 || !workspace) return FA_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return FA_ERR_MISALIGNED;
+    const int64_t BH = static_cast<int64_t>(B) * H;
+    if (workspace_bytes < splitkv_bytes(BH, Nq, d, num_splits)) return FA_ERR_INVALID_ARG;
+    float *O_part = static_cast<float *>(workspace);
+    float *LSE_part = reinterpret_cast<float *>(static_cast<char *>(workspace) + splitkv_o_bytes(BH, Nq, d, num_splits));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (num_splits == 1)   // one slice: the plain forward writes O and LSE itself
+        return run_forward(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, causal, 1, nullptr, nullptr, s);
+    st = run_forward(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, causal, num_splits, O_part, LSE_part, s);
+    if (st != FA_OK) return st;
+    return run_merge(O_part, LSE_part, O, LSE, BH * Nq, d, num_splits, s);
+}
+
+extern "C" fa_status fa_schedule(int B, int H, int Nq, int Nk, int d, int causal, int num_sms, int num_splits,
+                                 int32_t *items, int64_t capacity, int64_t *n_items) {
+    if (!n_items || num_sms < 1 || num_splits < 1 || num_splits > 256) return FA_ERR_INVALID_ARG;
     const float scale = 1.0f;
     char dummy[16] __attribute__((aligned(16)));
     fa_status st = validate(dummy, dummy, dummy, dummy, reinterpret_cast<float *>(dummy), B, H, Nq, Nk, d, scale);
     if (st != FA_OK) return st;
     fa::FwdParams p;
-    const int grid = setup_params(p, B, H, Nq, Nk, d, scale, causal, num_sms);
+    const int grid = setup_params(p, B, H, Nq, Nk, d, scale, causal, num_sms, num_splits);
     *n_items = p.n_items;
     if (!items) return FA_OK;
     if (capacity < p.n_items) return FA_ERR_INVALID_ARG;
@@ -197,8 +294,9 @@ extern "C" fa_status fa_schedule(int B, int H, int Nq, int Nk, int d, int causal
             const int w = fa::item_of_round(p, k, b, grid);
             if (w < 0) break;
             const fa::Item it = fa::decode_item(p, w);
-            int32_t *out = items + 6 * n++;
-            out[0] = b; out[1] = k; out[2] = it.bh; out[3] = it.q0; out[4] = it.nk[0]; out[5] = it.ntiles > 1 ? it.nk[1] : 0;
+            int32_t *out = items + 8 * n++;
+            out[0] = b; out[1] = k; out[2] = it.bh; out[3] = it.q0; out[4] = it.kv0;
+            out[5] = it.nk[0]; out[6] = it.ntiles > 1 ? it.nk[1] : -1; out[7] = it.split;
         }
     }
     return n == p.n_items ? FA_OK : FA_ERR_INVALID_ARG;

@@ -103,6 +103,9 @@ struct FwdParams {
     int n_pair_items;  // items [0, n_pair_items) are whole pairs
     int n_items;       // the rest are single tiles of the last pairs in order
     int heads_per_group;  // items are ordered by groups of heads (L2 locality)
+    int kv_splits;     // > 1: each item covers 1/kv_splits of its key range and writes partials
+    float *O_part;     // [kv_splits][BH][Nq][D] fp32 partial outputs (normalised by their own sum)
+    float *LSE_part;   // [kv_splits][BH][Nq] fp32 partial log-sum-exp (-inf: no visible key)
     int causal;
     float c2;          // scale * log2(e)
 };
@@ -111,16 +114,24 @@ struct Item {
     int bh;
     int q0;        // first query row of tile 0 of this item
     int ntiles;    // 1 or 2
-    int nk[2];     // K/V tiles visited by each tile (0 if absent)
+    int kv0;       // first K/V tile of the item's key range
+    int nk[2];     // one past the last K/V tile each query tile visits; a tile with
+                   // nk <= kv0 has nothing to do in this item
+    int split;     // index of the key-range slice (0 without splitting)
 };
 
 // Item w of the list.  Heads are taken in groups of heads_per_group whose
 // K/V fit in L2 together; inside a group, pairs go by descending pair index
-// (for causal the heaviest first), heads inner.  The last pairs of the list
-// (the lightest) are split into single-tile items.
+// (for causal the heaviest first), heads inner.  Without key splitting the
+// last pairs of the list (the lightest) are split into single-tile items;
+// with it, each pair appears kv_splits times in a row, once per slice of the
+// keys its tiles can see ("6. FlashAttention 分块逻辑" section 11: the key
+// blocks are processed independently and merged afterwards).
 __host__ __device__ __forceinline__ Item decode_item(const FwdParams &p, int w) {
-    int r, first, single;
-    if (w < p.n_pair_items) {
+    int r, first, single, split = 0;
+    if (p.kv_splits > 1) {
+        r = w / p.kv_splits; split = w - r * p.kv_splits; first = 0; single = 0;
+    } else if (w < p.n_pair_items) {
         r = w; first = 0; single = 0;
     } else {
         const int s = w - p.n_pair_items;
@@ -137,6 +148,7 @@ __host__ __device__ __forceinline__ Item decode_item(const FwdParams &p, int w) 
     it.q0 = (2 * pair + first) * kBR;
     const int left = p.Tr - (2 * pair + first);
     it.ntiles = single ? 1 : (left >= 2 ? 2 : 1);
+    int vis[2];
     #pragma unroll
     for (int t = 0; t < 2; ++t) {
         int nk = 0;
@@ -149,7 +161,19 @@ __host__ __device__ __forceinline__ Item decode_item(const FwdParams &p, int w) 
                 nk = need < p.Tc ? need : p.Tc;
             }
         }
-        it.nk[t] = nk;
+        vis[t] = nk;
+    }
+    it.split = split;
+    if (p.kv_splits > 1) {
+        const int nkv = vis[0] > vis[1] ? vis[0] : vis[1];
+        const int kb = split * nkv / p.kv_splits, ke = (split + 1) * nkv / p.kv_splits;
+        it.kv0 = kb;
+        #pragma unroll
+        for (int t = 0; t < 2; ++t) it.nk[t] = vis[t] < ke ? vis[t] : ke;
+    } else {
+        it.kv0 = 0;
+        it.nk[0] = vis[0];
+        it.nk[1] = vis[1];
     }
     return it;
 }
@@ -233,7 +257,7 @@ __device__ void producer_role(const FwdParams &p, const Shared &sh, uint32_t sme
                                  c * 64, item.q0 + t * kBR, item.bh, pol_q);
         const int nkv = max(item.nk[0], item.nk[1]);
         bool ok = true;
-        for (int j = 0; j < nkv && ok; ++j) {
+        for (int j = item.kv0; j < nkv && ok; ++j) {
             #pragma unroll 1
             for (int which = 0; which < 2; ++which, ++it) {
                 const uint32_t slot = it % C::kSlots;
@@ -303,26 +327,31 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
         const int w = item_of_round(p, k);
         if (w < 0) break;
         const Item item = decode_item(p, w);
-        const int nk0 = item.nk[0], nk1 = item.nk[1];
+        const int kv0 = item.kv0;
+        const int nk0 = item.nk[0], nk1 = item.nk[1];   // tile t is active for kv0 <= j < nk_t
         const int nkv = max(nk0, nk1);
         if (!wait_bar(sh.q_full, k & 1, sh.abort_flag, 1, w, -1)) return;
         ptx::tc_fence_after_sync();
+        if (nkv <= kv0) {   // an empty key slice: release Q and move on
+            ptx::mma_commit(sh.q_empty);
+            continue;
+        }
 
-        // S_t(0) for both tiles from K_0.
+        // S_t(kv0) for both tiles from the first K tile.
         uint32_t ks = it % C::kSlots;
-        if (!wait_bar(sh.kv_full0 + 8 * ks, (it / C::kSlots) & 1, sh.abort_flag, 1, w, 0)) return;
+        if (!wait_bar(sh.kv_full0 + 8 * ks, (it / C::kSlots) & 1, sh.abort_flag, 1, w, kv0)) return;
         ptx::tc_fence_after_sync();
         for (int t = 0; t < 2; ++t) {
-            if (item.nk[t] > 0) {
+            if (item.nk[t] > kv0) {
                 issue_s<D>(tS[t], sQ[t], smem_ring + ks * C::kKVTileBytes);
                 ptx::mma_commit(sh.s_full0 + 8 * t);
             }
         }
         ptx::mma_commit(sh.kv_empty0 + 8 * ks);
-        if (nkv == 1) ptx::mma_commit(sh.q_empty);
+        if (nkv == kv0 + 1) ptx::mma_commit(sh.q_empty);
         ++it;
 
-        for (int j = 0; j < nkv; ++j) {
+        for (int j = kv0; j < nkv; ++j) {
             const uint32_t vs = it % C::kSlots;
             if (!wait_bar(sh.kv_full0 + 8 * vs, (it / C::kSlots) & 1, sh.abort_flag, 1, w, j)) return;
             ptx::tc_fence_after_sync();
@@ -335,7 +364,7 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
                 if (!wait_bar(sh.p_full0, p_phase[0], sh.abort_flag, 1, w, j)) return;
                 p_phase[0] ^= 1u;
                 ptx::tc_fence_after_sync();
-                issue_pv<D>(tO[0], tS[0], v_tile, j > 0);
+                issue_pv<D>(tO[0], tS[0], v_tile, j > kv0);
                 if (j == nk0 - 1) ptx::mma_commit(sh.o_full0);
             }
             if (more) {
@@ -351,7 +380,7 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
                 if (!wait_bar(sh.p_full0 + 8, p_phase[1], sh.abort_flag, 1, w, j)) return;
                 p_phase[1] ^= 1u;
                 ptx::tc_fence_after_sync();
-                issue_pv<D>(tO[1], tS[1], v_tile, j > 0);
+                issue_pv<D>(tO[1], tS[1], v_tile, j > kv0);
                 if (j == nk1 - 1) ptx::mma_commit(sh.o_full0 + 8);
             }
             ptx::mma_commit(sh.kv_empty0 + 8 * vs);
@@ -458,12 +487,17 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
         if (tile >= item.ntiles) continue;
         const int nk = item.nk[tile];
         const int qg = item.q0 + tile * kBR + row;   // this thread's query row
+        const size_t prow = (static_cast<size_t>(item.split) * p.BH + item.bh) * p.Nq + qg;   // partial row
+        if (nk <= item.kv0) {   // no visible key in this slice: an empty partial
+            if (qg < p.Nq) p.LSE_part[prow] = -INFINITY;
+            continue;
+        }
         const int key_lim = p.causal ? min(p.Nk, qg + 1) : p.Nk;
         float m_ref = -INFINITY;   // log2-domain reference maximum
         float l = 0.f;             // sum of p (fp32), for LSE
         float l_rounded = 0.f;     // sum of the bf16 p that P V uses, for O
 
-        for (int j = 0; j < nk; ++j) {
+        for (int j = item.kv0; j < nk; ++j) {
             if (!wait_bar(sh.s_full0 + 8 * tile, s_phase, sh.abort_flag, 2 + tile, w, j)) return;
             s_phase ^= 1u;
             ptx::tc_fence_after_sync();
@@ -493,7 +527,7 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
             l_rounded += sr;
             // Rescale O_t in TMEM when this warp's reference maximum moved
             // (PV_t(j-1) has completed, see the header; PV_t(j) waits for us).
-            if (__any_sync(0xffffffffu, j > 0 && alpha != 1.f)) {
+            if (__any_sync(0xffffffffu, j > item.kv0 && alpha != 1.f)) {
                 #pragma unroll 1
                 for (int ch = 0; ch < D / 32; ++ch) {
                     uint32_t o[32];
@@ -514,23 +548,43 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
         ptx::tc_fence_after_sync();
         const float inv_l = 1.f / l_rounded;
         const bool live = qg < p.Nq;
-        __nv_bfloat16 *orow = p.O + (static_cast<size_t>(item.bh) * p.Nq + qg) * D;
-        #pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t o[32];
-            ptx::tmem_load_32cols(tO + ch * 32, o);
-            uint32_t h[16];
-            #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                h[i] = ptx::pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-            if (live) {
-                // streaming stores: O is written once, keep L2 for K/V
-                uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
-                #pragma unroll
-                for (int i = 0; i < 4; ++i) __stcs(dst + i, make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]));
+        const float lse = (m_ref + ptx::lg2(l)) * 0.69314718055994531f;
+        if (p.kv_splits > 1) {
+            // partial of this key slice: O / l in fp32 and its LSE
+            float *prow_o = p.O_part + prow * D;
+            #pragma unroll 1
+            for (int ch = 0; ch < D / 32; ++ch) {
+                uint32_t o[32];
+                ptx::tmem_load_32cols(tO + ch * 32, o);
+                if (live) {
+                    float4 *dst = reinterpret_cast<float4 *>(prow_o + ch * 32);
+                    #pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        __stcs(dst + i, make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                                    __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l));
+                }
             }
+            if (live) p.LSE_part[prow] = lse;
+        } else {
+            __nv_bfloat16 *orow = p.O + (static_cast<size_t>(item.bh) * p.Nq + qg) * D;
+            #pragma unroll 1
+            for (int ch = 0; ch < D / 32; ++ch) {
+                uint32_t o[32];
+                ptx::tmem_load_32cols(tO + ch * 32, o);
+                uint32_t h[16];
+                #pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    h[i] = ptx::pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+                if (live) {
+                    // streaming stores: O is written once, keep L2 for K/V
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
+                    #pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        __stcs(dst + i, make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]));
+                }
+            }
+            if (live) p.LSE[static_cast<size_t>(item.bh) * p.Nq + qg] = lse;
         }
-        if (live) p.LSE[static_cast<size_t>(item.bh) * p.Nq + qg] = (m_ref + ptx::lg2(l)) * 0.69314718055994531f;
         ptx::tc_fence_before_sync();
     }
 }
@@ -632,6 +686,46 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         ptx::tc_fence_after_sync();
         ptx::tmem_dealloc(tmem, C::kTmemCols);
     }
+}
+
+// ---------------------------------------------------------- split-KV merge
+//
+// Combines the kv_splits partial results of each query row with the
+// online-softmax merge of "6. FlashAttention 分块逻辑" sections 11.3 and 13.2:
+// with partial outputs O_s (already divided by their own sums) and
+// LSE_s = m_s + ln l_s, the merged row is
+//   m = max_s LSE_s,  w_s = exp(LSE_s - m),  O = sum_s w_s O_s / sum_s w_s,
+//   LSE = m + ln sum_s w_s.
+// One warp per row; lane c holds columns c, c+32, ...  Empty partials
+// (LSE_s = -inf) carry no weight and are not read.
+template <int D>
+__global__ void __launch_bounds__(256) fa_merge_kernel(const float *__restrict__ O_part,
+                                                       const float *__restrict__ LSE_part,
+                                                       __nv_bfloat16 *__restrict__ O, float *__restrict__ LSE,
+                                                       long long rows, int splits) {
+    const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const int lane = threadIdx.x & 31;
+    float m = -INFINITY;
+    for (int s = 0; s < splits; ++s) m = fmaxf(m, LSE_part[s * rows + row]);
+    float acc[D / 32];
+    #pragma unroll
+    for (int c = 0; c < D / 32; ++c) acc[c] = 0.f;
+    float wsum = 0.f;
+    for (int s = 0; s < splits; ++s) {
+        const float lse = LSE_part[s * rows + row];
+        if (lse == -INFINITY) continue;
+        const float w = expf(lse - m);
+        wsum += w;
+        const float *src = O_part + (s * rows + row) * D;
+        #pragma unroll
+        for (int c = 0; c < D / 32; ++c) acc[c] = fmaf(w, src[lane + 32 * c], acc[c]);
+    }
+    const float inv = 1.f / wsum;
+    __nv_bfloat16 *dst = O + row * D;
+    #pragma unroll
+    for (int c = 0; c < D / 32; ++c) dst[lane + 32 * c] = __float2bfloat16_rn(acc[c] * inv);
+    if (lane == 0) LSE[row] = m + logf(wsum);
 }
 
 }  // namespace fa

@@ -39,9 +39,13 @@ def load_library(path: str | None = None):
     lib.fa_fwd.restype = i
     lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
     lib.fa_fwd_host.restype = i
+    lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, ctypes.c_size_t, vp]
+    lib.fa_fwd_splitkv.restype = i
+    lib.fa_splitkv_workspace.argtypes = [i, i, i, i, i, i, vp, vp]
+    lib.fa_splitkv_workspace.restype = i
     lib.fa_check_device_status.argtypes = [vp]
     lib.fa_check_device_status.restype = i
-    lib.fa_schedule.argtypes = [i, i, i, i, i, i, i, vp, ctypes.c_int64, vp]
+    lib.fa_schedule.argtypes = [i, i, i, i, i, i, i, i, vp, ctypes.c_int64, vp]
     lib.fa_schedule.restype = i
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
@@ -108,16 +112,45 @@ def check_device_status(stream=None):
     _check(load_library().fa_check_device_status(_stream_handle(stream)))
 
 
-def schedule(B, H, Nq, Nk, d, causal, num_sms):
-    """The kernel's work list: int32 array [n_items, 6] of
-    (cta, round, batch*head, first query row, KV tiles of tile 0, of tile 1)."""
+def schedule(B, H, Nq, Nk, d, causal, num_sms, num_splits=1):
+    """The kernel's work list: int32 array [n_items, 8] of (cta, round,
+    batch*head, first query row, first KV tile, end KV tile of query tile 0,
+    of query tile 1 (-1 if absent), key slice)."""
     import numpy as np
     lib = load_library()
     n = ctypes.c_int64(0)
-    _check(lib.fa_schedule(B, H, Nq, Nk, d, int(bool(causal)), num_sms, None, 0, ctypes.byref(n)))
-    out = np.zeros((n.value, 6), dtype=np.int32)
-    _check(lib.fa_schedule(B, H, Nq, Nk, d, int(bool(causal)), num_sms, out.ctypes.data, n.value, ctypes.byref(n)))
+    args = (B, H, Nq, Nk, d, int(bool(causal)), num_sms, num_splits)
+    _check(lib.fa_schedule(*args, None, 0, ctypes.byref(n)))
+    out = np.zeros((n.value, 8), dtype=np.int32)
+    _check(lib.fa_schedule(*args, out.ctypes.data, n.value, ctypes.byref(n)))
     return out
+
+
+def splitkv_workspace(B, H, Nq, Nk, d, causal=False, num_splits=0):
+    """(num_splits, workspace bytes) for fa_fwd_splitkv; num_splits=0 lets the library choose."""
+    ns = ctypes.c_int(num_splits)
+    nb = ctypes.c_size_t(0)
+    _check(load_library().fa_splitkv_workspace(B, H, Nq, Nk, d, int(bool(causal)), ctypes.byref(ns), ctypes.byref(nb)))
+    return ns.value, nb.value
+
+
+def fa_fwd_splitkv(q, k, v, o=None, lse=None, scale=None, causal=False, num_splits=0, workspace=None,
+                   stream=None):
+    """Split-key attention forward; `workspace` is a CUDA uint8 tensor (allocated here if None)."""
+    B, H, Nq, Nk, d = _shape(q, k)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    num_splits, nbytes = splitkv_workspace(B, H, Nq, Nk, d, causal, num_splits)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    _check(load_library().fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                         B, H, Nq, Nk, d, scale, int(bool(causal)), num_splits,
+                                         workspace.data_ptr(), workspace.numel(), _stream_handle(stream)))
+    return o, lse
 
 
 def raw_fa_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Nq, Nk, d, scale, causal, stream_handle=0) -> int:

@@ -26,6 +26,7 @@
 #ifndef FA_GB300_H
 #define FA_GB300_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -92,22 +93,63 @@ fa_status fa_fwd_host(const void *hQ, const void *hK, const void *hV, void *hO, 
 fa_status fa_check_device_status(fa_stream_t stream);
 
 /*
- * fa_schedule -- the work list fa_fwd would run for these shapes on a GPU
- * with num_sms SMs (host only; no GPU needed).  The kernel's persistent CTAs
- * each walk this list; a work item is one (batch*head, pair of 128-row query
- * tiles) or a single tile, in the order "9.4 FlashAttention 与 FlashMLA"
- * section 9.4.4 describes for FA2: parallel over batch x heads x query
- * blocks, each block looping over all key/value blocks it can see.
+ * fa_fwd_splitkv -- the same operation with each query tile's key range cut
+ * into num_splits slices that run as independent work items, followed by a
+ * merge ("6. FlashAttention 分块逻辑", section 11: FlashDecoding -- key/value
+ * blocks processed in parallel, each keeping its own max and sum, then
+ * reduced; section 13.2: the correct merge of (m, l, o) triples).  It gives
+ * short-query / long-key shapes (decoding) enough parallel work to fill the
+ * GPU.
  *
- *   items     int32 [capacity][6], caller-owned, may be NULL to only count:
- *             {cta, round, batch*head, first query row, KV tiles of query tile 0,
- *              KV tiles of query tile 1 (0 if the item holds one tile)}
+ *   Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, causal: as fa_fwd
+ *   num_splits   1..256 slices (fa_splitkv_workspace picks one when asked)
+ *   workspace    caller-owned device memory, 256-byte aligned, at least the
+ *                size fa_splitkv_workspace returns; holds the fp32 partial
+ *                outputs [num_splits][B*H][Nq][d] and partial LSE
+ *                [num_splits][B*H][Nq]; contents on entry are ignored and are
+ *                undefined afterwards
+ *   stream       both kernels (partials, merge) are enqueued on it
+ *
+ * Errors: as fa_fwd; FA_ERR_INVALID_ARG also for num_splits out of range, a
+ * NULL or too small workspace; FA_ERR_MISALIGNED for a workspace not 256-byte
+ * aligned.  Two calls sharing a workspace must not overlap in time.
+ */
+fa_status fa_fwd_splitkv(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                         int B, int H, int Nq, int Nk, int d, float scale, int causal, int num_splits,
+                         void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
+ * fa_splitkv_workspace -- workspace bytes fa_fwd_splitkv needs.  *num_splits
+ * = 0 asks for the library's choice for the current device: 1 (no
+ * splitting) unless the unsplit work list would keep at most half of the SMs
+ * busy, else about one work item per SM, at most one slice per 128-key tile
+ * and at most 64 (this reads the device's SM count); any other value is used
+ * as given.  No allocation and no GPU work; with *num_splits > 0 no GPU is
+ * needed at all.  With one slice fa_fwd_splitkv is fa_fwd and does not touch
+ * the workspace.
+ */
+fa_status fa_splitkv_workspace(int B, int H, int Nq, int Nk, int d, int causal, int *num_splits,
+                               size_t *bytes);
+
+/*
+ * fa_schedule -- the work list fa_fwd (num_splits = 1) or fa_fwd_splitkv
+ * would run for these shapes on a GPU with num_sms SMs (host only; no GPU
+ * needed).  The kernel's persistent CTAs each walk this list; a work item is
+ * one (batch*head, pair of 128-row query tiles) or a single tile, over all
+ * the key/value tiles it can see or one slice of them -- the parallelisation
+ * over batch x heads x query blocks that "9.4 FlashAttention 与 FlashMLA"
+ * section 9.4.4 describes for FA2.
+ *
+ *   items     int32 [capacity][8], caller-owned, may be NULL to only count:
+ *             {cta, round, batch*head, first query row, first KV tile,
+ *              end KV tile of query tile 0, end KV tile of query tile 1 (-1 if
+ *              the item holds one tile), key slice index}
  *   n_items   out: number of items
  * Returns FA_ERR_INVALID_ARG for bad sizes or capacity < *n_items (after
  * setting *n_items), FA_ERR_UNSUPPORTED for d not in {64, 128}.
  */
-fa_status fa_schedule(int B, int H, int Nq, int Nk, int d, int causal, int num_sms, int32_t *items,
-                      int64_t capacity, int64_t *n_items);
+fa_status fa_schedule(int B, int H, int Nq, int Nk, int d, int causal, int num_sms, int num_splits,
+                      int32_t *items, int64_t capacity, int64_t *n_items);
 
 /* A static, human-readable name for a status code (never NULL). */
 const char *fa_status_string(fa_status s);

@@ -81,6 +81,20 @@ def test_argument_errors_before_any_launch(lib, kw, expected):
     assert call(**kw) == expected
 
 
+@pytest.mark.parametrize("splits,ws,nbytes,expected", [
+    (0, 0x100000, 1 << 30, ops.FA_ERR_INVALID_ARG),      # num_splits < 1
+    (257, 0x100000, 1 << 30, ops.FA_ERR_INVALID_ARG),    # num_splits > 256
+    (2, 0, 1 << 30, ops.FA_ERR_INVALID_ARG),             # NULL workspace
+    (2, 0x100010, 1 << 30, ops.FA_ERR_MISALIGNED),       # not 256-byte aligned
+    (2, 0x100000, 64, ops.FA_ERR_INVALID_ARG),           # too small
+])
+def test_splitkv_argument_errors(lib, splits, ws, nbytes, expected):
+    a = GOOD
+    st = lib.fa_fwd_splitkv(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"], a["Nk"], a["d"],
+                            a["scale"], a["causal"], splits, ws, nbytes, None)
+    assert st == expected
+
+
 def test_host_entry_rejects_null_host_buffers(lib):
     vp = ctypes.c_void_p
     st = lib.fa_fwd_host(None, vp(1 << 16), vp(1 << 16), vp(1 << 16), vp(1 << 16),

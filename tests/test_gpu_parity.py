@@ -234,3 +234,44 @@ def test_host_buffer_entry_point(ops):
     ops.check_device_status()
     O_ref, L_ref = oracle.attention(q, k, v, 0.088, False)
     assert_close(ho, hl, O_ref, L_ref, "host entry")
+
+
+# ------------------------------------------------------------- split keys
+
+def run_split(ops, q, k, v, scale, causal, splits):
+    o, lse = ops.fa_fwd_splitkv(to_dev(q), to_dev(k), to_dev(v), scale=scale, causal=causal, num_splits=splits)
+    ops.check_device_status()
+    return o, lse
+
+
+@pytest.mark.parametrize("name", ["b8_h32_q128_kv8192_d128", "b8_h32_q128_kv8229_d128"])
+def test_split_keys_short_query_long_key_workloads(ops, name):
+    w = inputs.WORKLOADS[name]
+    q, k, v, scale = inputs.make_inputs(w)
+    o, lse = run_split(ops, q, k, v, scale, w.causal, 0)
+    rows = sample_rows(w.B, w.H, w.Nq, seed=w.index)
+    O_ref, L_ref = oracle.attention_rows(q, k, v, scale, w.causal, rows=rows)
+    idx = torch.from_numpy(rows).cuda()
+    assert_close(o.reshape(-1, w.d)[idx], lse.reshape(-1)[idx], O_ref, L_ref, name)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 64])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq,Nk,d", [(1, 4096, 128), (16, 1000, 64), (300, 1500, 128), (640, 129, 64), (1, 1, 128)])
+def test_split_keys_against_oracle(ops, splits, causal, Nq, Nk, d):
+    q, k, v = inputs.custom_inputs(9000 + Nq + Nk, 2, 3, Nq, Nk, d)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    o, lse = run_split(ops, q, k, v, scale, causal, splits)
+    O_ref, L_ref = oracle.attention(q, k, v, scale, causal)
+    assert_close(o, lse, O_ref, L_ref, f"splits={splits} {Nq}x{Nk}x{d} causal={causal}")
+
+
+def test_split_keys_decode_shape_auto(ops):
+    # one query per head against a long cache: 32 work items without splitting
+    B, H, Nq, Nk, d = 1, 32, 1, 32768, 128
+    q, k, v = inputs.custom_inputs(31, B, H, Nq, Nk, d)
+    ns, _ = ops.splitkv_workspace(B, H, Nq, Nk, d, False, 0)
+    assert ns > 1
+    o, lse = run_split(ops, q, k, v, 0.088, False, 0)
+    O_ref, L_ref = oracle.attention(q, k, v, 0.088, False)
+    assert_close(o, lse, O_ref, L_ref, "decode")

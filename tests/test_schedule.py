@@ -20,13 +20,18 @@ def lib():
 
 
 def expand(items):
-    """(cta, round, bh, q0, nk0, nk1) -> list of (bh, q_start, nk)."""
+    """(cta, round, bh, q0, kv0, end0, end1, split) -> list of (bh, q_start, kv0, end, split)."""
     tiles = []
-    for cta, rnd, bh, q0, nk0, nk1 in items.tolist():
-        tiles.append((bh, q0, nk0))
-        if nk1 > 0:
-            tiles.append((bh, q0 + 128, nk1))
+    for cta, rnd, bh, q0, kv0, e0, e1, split in items.tolist():
+        tiles.append((bh, q0, kv0, e0, split))
+        if e1 >= 0:                      # -1: the item holds one query tile
+            tiles.append((bh, q0 + 128, kv0, e1, split))
     return tiles
+
+
+def visible_tiles(Nq, Nk, causal, q):
+    Tc = math.ceil(Nk / 128)
+    return min(Tc, (min(Nq, q + 128) - 1) // 128 + 1) if causal else Tc
 
 
 SHAPES = [
@@ -42,13 +47,12 @@ SHAPES = [
 def test_every_tile_exactly_once_with_its_kv_range(B, H, Nq, Nk, d, causal, sms):
     items = ops.schedule(B, H, Nq, Nk, d, causal, sms)
     tiles = expand(items)
-    Tr, Tc = math.ceil(Nq / 128), math.ceil(Nk / 128)
+    Tr = math.ceil(Nq / 128)
     assert len(tiles) == B * H * Tr
-    assert len(set((bh, q) for bh, q, _ in tiles)) == B * H * Tr
-    for bh, q, nk in tiles:
-        assert 0 <= bh < B * H and q % 128 == 0 and q < Nq
-        want = min(Tc, (min(Nq, q + 128) - 1) // 128 + 1) if causal else Tc
-        assert nk == want, (bh, q, nk, want)
+    assert len(set((bh, q) for bh, q, *_ in tiles)) == B * H * Tr
+    for bh, q, kv0, end, split in tiles:
+        assert 0 <= bh < B * H and q % 128 == 0 and q < Nq and kv0 == 0 and split == 0
+        assert end == visible_tiles(Nq, Nk, causal, q), (bh, q, end)
     # each CTA walks consecutive rounds 0, 1, 2, ...
     for cta in np.unique(items[:, 0]):
         rounds = np.sort(items[items[:, 0] == cta, 1])
@@ -56,10 +60,26 @@ def test_every_tile_exactly_once_with_its_kv_range(B, H, Nq, Nk, d, causal, sms)
     assert items[:, 0].max() < sms
 
 
+@pytest.mark.parametrize("B,H,Nq,Nk,d,causal", SHAPES)
+@pytest.mark.parametrize("splits", [2, 3, 8, 64])
+def test_key_slices_partition_each_tiles_range(B, H, Nq, Nk, d, causal, splits):
+    items = ops.schedule(B, H, Nq, Nk, d, causal, 152, splits)
+    by_tile = {}
+    for bh, q, kv0, end, split in expand(items):
+        by_tile.setdefault((bh, q), []).append((split, kv0, end))
+    assert len(by_tile) == B * H * math.ceil(Nq / 128)
+    for (bh, q), parts in by_tile.items():
+        assert sorted(s for s, _, _ in parts) == list(range(splits))   # every slice once
+        covered = []
+        for _, kv0, end in parts:
+            covered.extend(range(kv0, max(kv0, end)))
+        assert sorted(covered) == list(range(visible_tiles(Nq, Nk, causal, q))), (bh, q)
+
+
 def cta_loads(items, key=lambda nk: 1):
     load = {}
-    for cta, _, _, _, nk0, nk1 in items.tolist():
-        load[cta] = load.get(cta, 0) + key(nk0) + (key(nk1) if nk1 else 0)
+    for cta, _, _, _, kv0, nk0, nk1, _ in items.tolist():
+        load[cta] = load.get(cta, 0) + key(nk0 - kv0) + (key(nk1 - kv0) if nk1 >= 0 else 0)
     return np.array(list(load.values()), dtype=np.float64)
 
 
@@ -79,6 +99,13 @@ def test_causal_load_balance():
 def test_schedule_argument_errors():
     n = ops.ctypes.c_int64(0)
     lib = ops.load_library()
-    assert lib.fa_schedule(1, 1, 128, 128, 96, 0, 152, None, 0, ops.ctypes.byref(n)) == ops.FA_ERR_UNSUPPORTED
-    assert lib.fa_schedule(0, 1, 128, 128, 64, 0, 152, None, 0, ops.ctypes.byref(n)) == ops.FA_ERR_INVALID_ARG
-    assert lib.fa_schedule(1, 1, 128, 128, 64, 0, 0, None, 0, ops.ctypes.byref(n)) == ops.FA_ERR_INVALID_ARG
+    assert lib.fa_schedule(1, 1, 128, 128, 96, 0, 152, 1, None, 0, ops.ctypes.byref(n)) == ops.FA_ERR_UNSUPPORTED
+    assert lib.fa_schedule(0, 1, 128, 128, 64, 0, 152, 1, None, 0, ops.ctypes.byref(n)) == ops.FA_ERR_INVALID_ARG
+    assert lib.fa_schedule(1, 1, 128, 128, 64, 0, 0, 1, None, 0, ops.ctypes.byref(n)) == ops.FA_ERR_INVALID_ARG
+    assert lib.fa_schedule(1, 1, 128, 128, 64, 0, 152, 0, None, 0, ops.ctypes.byref(n)) == ops.FA_ERR_INVALID_ARG
+
+
+def test_splitkv_workspace_size():
+    ns, nb = ops.splitkv_workspace(8, 32, 128, 8192, 128, False, num_splits=4)
+    o_bytes = 4 * 8 * 32 * 128 * 128 * 4
+    assert ns == 4 and nb == o_bytes + 4 * 8 * 32 * 128 * 4
