@@ -323,6 +323,70 @@ extern "C" fa_status fa_fwd_host(const void *hQ, const void *hK, const void *hV,
     return FA_OK;
 }
 
+// ------------------------------------------------- split keys without allocating
+//
+// Some callers cannot allocate device memory where they call attention: code
+// being recorded into a CUDA graph (an allocation there is not replayed and
+// cudaMalloc may synchronise the device), serving loops with a latency budget
+// that rules out the allocator, frameworks whose allocator owns all memory up
+// front, and plugins handed only the tensors they read and write.  For them the
+// split-key forward can put its partial results in a scratch area that lives in
+// this file: a fixed array in device global memory, which every GPU that loads
+// the library holds until the process exits.  Its host-side name is only a
+// stand-in; the device address is looked up once per device.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t{16} << 20;   // 16 MiB on each GPU
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+void *g_noalloc_addr[64];   // device address of g_noalloc_scratch, per device
+
+// Device address of the scratch array on the current device (looked up on the
+// first call on that device).
+fa_status noalloc_scratch(void *&addr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (!g_noalloc_addr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return FA_ERR_CUDA;
+        g_noalloc_addr[dev] = ptr;
+    }
+    addr = g_noalloc_addr[dev];
+    return FA_OK;
+}
+
+}  // namespace
+
+extern "C" fa_status fa_fwd_splitkv_noalloc(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
+                                            int H, int Nq, int Nk, int d, float scale, int causal, int num_splits,
+                                            fa_stream_t stream) {
+    fa_status st = validate(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale);
+    if (st != FA_OK) return st;
+    if (num_splits < 0 || num_splits > 256) return FA_ERR_INVALID_ARG;
+    const int64_t BH = static_cast<int64_t>(B) * H;
+    if (num_splits == 0) {
+        int sms;
+        bool *attr_done;
+        st = device_info(d, sms, attr_done);
+        if (st != FA_OK) return st;
+        num_splits = choose_splits(BH, Nq, Nk, sms);
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (num_splits == 1)   // one slice: no partials, no scratch
+        return run_forward(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, causal, 1, nullptr, nullptr, s);
+    if (splitkv_bytes(BH, Nq, d, num_splits) > kNoAllocScratchBytes) return FA_ERR_TOO_LARGE;
+    void *scratch = nullptr;
+    st = noalloc_scratch(scratch);
+    if (st != FA_OK) return st;
+    // Nothing needs clearing: the forward writes every partial the merge reads.
+    float *O_part = static_cast<float *>(scratch);
+    float *LSE_part = reinterpret_cast<float *>(static_cast<char *>(scratch) + splitkv_o_bytes(BH, Nq, d, num_splits));
+    st = run_forward(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, causal, num_splits, O_part, LSE_part, s);
+    if (st != FA_OK) return st;
+    return run_merge(O_part, LSE_part, O, LSE, BH * Nq, d, num_splits, s);
+}
+
 extern "C" fa_status fa_check_device_status(fa_stream_t stream) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
     unsigned int status = 0;
@@ -341,6 +405,8 @@ extern "C" const char *fa_status_string(fa_status s) {
     case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED: Q, K, V, O need 16-byte alignment, LSE 4-byte";
     case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel wait expired; outputs are undefined";
+    case FA_ERR_TOO_LARGE:
+        return "FA_ERR_TOO_LARGE: the partial results need more than the library's fixed 16 MiB scratch area";
     }
     return "unknown fa_status";
 }

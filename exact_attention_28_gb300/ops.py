@@ -13,7 +13,8 @@ import torch
 
 from .build import LIB_PATH
 
-FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(6)
+(FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED, FA_ERR_CUDA, FA_ERR_TIMEOUT,
+ FA_ERR_TOO_LARGE) = range(7)
 
 _lib = None
 
@@ -41,6 +42,8 @@ def load_library(path: str | None = None):
     lib.fa_fwd_host.restype = i
     lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, ctypes.c_size_t, vp]
     lib.fa_fwd_splitkv.restype = i
+    lib.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
+    lib.fa_fwd_splitkv_noalloc.restype = i
     lib.fa_splitkv_workspace.argtypes = [i, i, i, i, i, i, vp, vp]
     lib.fa_splitkv_workspace.restype = i
     lib.fa_check_device_status.argtypes = [vp]
@@ -150,6 +153,18 @@ def fa_fwd_splitkv(q, k, v, o=None, lse=None, scale=None, causal=False, num_spli
     _check(load_library().fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                                          B, H, Nq, Nk, d, scale, int(bool(causal)), num_splits,
                                          workspace.data_ptr(), workspace.numel(), _stream_handle(stream)))
+    return o, lse
+
+
+def fa_fwd_splitkv_noalloc(q, k, v, o, lse, scale=None, causal=False, num_splits=0, stream=None):
+    """Split-key forward whose partials live in the library's fixed scratch area
+    (no allocation anywhere on this call; o and lse are caller-provided)."""
+    B, H, Nq, Nk, d = _shape(q, k)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _check(load_library().fa_fwd_splitkv_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                                 lse.data_ptr(), B, H, Nq, Nk, d, scale, int(bool(causal)),
+                                                 num_splits, _stream_handle(stream)))
     return o, lse
 
 

@@ -42,7 +42,8 @@ typedef enum {
     FA_ERR_UNSUPPORTED = 2,  /* head dimension d other than 64 or 128 */
     FA_ERR_MISALIGNED = 3,   /* Q, K, V or O not 16-byte aligned, or LSE not 4-byte aligned */
     FA_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed (launch, copy, encode) */
-    FA_ERR_TIMEOUT = 5       /* a kernel wait ran past its limit (see fa_check_device_status) */
+    FA_ERR_TIMEOUT = 5,      /* a kernel wait ran past its limit (see fa_check_device_status) */
+    FA_ERR_TOO_LARGE = 6     /* more scratch than fa_fwd_splitkv_noalloc's fixed area holds */
 } fa_status;
 
 /*
@@ -130,6 +131,37 @@ fa_status fa_fwd_splitkv(const void *Q, const void *K, const void *V, void *O, f
  */
 fa_status fa_splitkv_workspace(int B, int H, int Nq, int Nk, int d, int causal, int *num_splits,
                                size_t *bytes);
+
+/*
+ * fa_fwd_splitkv_noalloc -- fa_fwd_splitkv for callers that cannot allocate
+ * device memory: code being recorded into a CUDA graph (an allocation is not
+ * replayed, and cudaMalloc may synchronise the device), serving loops whose
+ * latency budget rules out the allocator, frameworks whose allocator owns all
+ * memory up front, plugins handed only their input and output tensors.  The
+ * pages have no counterpart; this is a property of the library, not of the
+ * method.
+ *
+ * The partial results go to a scratch area inside the library: a fixed
+ * 16 MiB array in device memory that every GPU loading the library holds
+ * until the process exits.  The call allocates nothing (no cudaMalloc, no
+ * cudaFree, no allocating library routine).  The caller still passes Q, K, V,
+ * O and LSE, with the meaning, layout and errors of fa_fwd_splitkv;
+ * num_splits = 0 lets the library choose, as fa_splitkv_workspace does.
+ *
+ *   - Limit: num_splits * B * H * Nq * (d + 1) * 4 bytes (plus alignment) must
+ *     fit in 16 MiB, else FA_ERR_TOO_LARGE and nothing is enqueued.  One slice
+ *     needs no scratch at all.
+ *   - The first call on a device looks up the device address of the scratch
+ *     array (cudaGetSymbolAddress, with that device current); make that first
+ *     call before any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind; nothing needs clearing, since each call writes every partial it
+ *     reads.  Calls whose kernels overlap on the GPU (different streams without
+ *     ordering between them) race on the array and give undefined results.
+ */
+fa_status fa_fwd_splitkv_noalloc(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                                 int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                                 int num_splits, fa_stream_t stream);
 
 /*
  * fa_schedule -- the work list fa_fwd (num_splits = 1) or fa_fwd_splitkv
