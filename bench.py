@@ -220,8 +220,9 @@ def run_reference(args, w):
     return 0
 
 
-def workload_config(w, l2_note):
+def workload_config(w, l2_note, args=None):
     cfg = {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": w.causal,
+           "path": getattr(args, "path", "fwd") if args is not None else "fwd",
            "sigma_qkv": [w.sigma_q, w.sigma_k, w.sigma_v], "scale": "1/sqrt(d) as fp32",
            "global_batch": w.B, "seq_len": w.Nq, "parallelism": "independent replicas (weak)"}
     if l2_note:
@@ -279,9 +280,19 @@ def run_ours(args, w):
                if n_sets > 1 else f"inputs {set_bytes / 2**20:.0f} MiB > 2x L2")
     stream = torch.cuda.current_stream()
 
+    workspace = None
+    splits = 1
+    if args.path == "splitkv":
+        splits, nbytes = ops.splitkv_workspace(w.B, w.H, w.Nq, w.Nk, w.d, w.causal, 0)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+
     def step(i):
         s = sets[i % n_sets]
-        ops.fa_fwd(s[0], s[1], s[2], s[3], s[4], scale=scale, causal=w.causal, stream=stream)
+        if args.path == "splitkv":
+            ops.fa_fwd_splitkv(s[0], s[1], s[2], s[3], s[4], scale=scale, causal=w.causal, num_splits=splits,
+                               workspace=workspace, stream=stream)
+        else:
+            ops.fa_fwd(s[0], s[1], s[2], s[3], s[4], scale=scale, causal=w.causal, stream=stream)
 
     for i in range(args.warmup):
         step(i)
@@ -322,25 +333,33 @@ def run_ours(args, w):
         peaks, peak_src = measured_peaks()
         ms_per_step = total_ms / args.steps
         value = aggregate_tflops(w.flops, ms_per_step, world)
-        achieved = w.flops / (launch_ms * 1e-3) / 1e12
-        peak = float(peaks["bf16_tflops"])
-        traffic = profiled_traffic()
+        ridge = float(peaks["bf16_tflops"]) * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
+        tensor_bound = w.flops / w.algorithmic_bytes >= ridge
+        if tensor_bound:
+            achieved, peak, unit, bound = w.flops / (launch_ms * 1e-3) / 1e12, float(peaks["bf16_tflops"]), \
+                "TFLOP/s", "tensor"
+        else:
+            achieved, peak, unit, bound = w.algorithmic_bytes / (launch_ms * 1e-3) / 1e9, float(peaks["hbm_gbs"]), \
+                "GB/s", "hbm"
+        traffic = profiled_traffic() if (w.name == DEFAULT_WORKLOAD and args.path == "fwd") else None
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0, sigma^2) rounded to bf16)",
-            "config": workload_config(w, l2_note),
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "config": dict(workload_config(w, l2_note, args), kv_splits=splits),
+            "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                          "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": f"{peak_src} bf16_tflops (burst)",
-                         "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
-                         "kernel": "fa_fwd_kernel<%d>" % w.d, "launch_ms": launch_ms},
+                         "peak_source": f"{peak_src} " + ("bf16_tflops (burst)" if tensor_bound else "hbm_gbs"),
+                         "frac_of_sustained": (achieved / float(peaks.get("bf16_tflops_sustained", peak))
+                                               if tensor_bound else None),
+                         "kernel": "fa_fwd_kernel<%d>" % w.d + (" + fa_merge_kernel" if splits > 1 else ""),
+                         "launch_ms": launch_ms},
             "e2e": None if args.no_e2e else {
                 "value": aggregate_tflops(w.flops, e2e_ms, world), "unit": "TFLOPS",
                 "h2d_bytes_per_step": 2 * (hq.numel() + 2 * hk.numel()),
                 "d2h_bytes_per_step": 2 * hq.numel() + 4 * w.B * w.H * w.Nq,
                 "ms_per_step": e2e_ms},
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * (2 if splits > 1 else 1),
             "clocks": sampler.summary(t0, t1) if sampler else None,
         }
         if world == 1 and not args.no_cpu_baseline:
@@ -364,6 +383,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
+    ap.add_argument("--path", choices=["fwd", "splitkv"], default="fwd",
+                    help="fa_fwd, or fa_fwd_splitkv with the library's slice count")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

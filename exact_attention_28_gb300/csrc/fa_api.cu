@@ -136,13 +136,14 @@ int setup_params(fa::FwdParams &p, int B, int H, int Nq, int Nk, int d, float sc
 
 // Key-range slices for the split path.  Splitting costs a partial write, a
 // merge and a re-read per slice, so it pays only when the unsplit work list
-// leaves most SMs idle (at most half of them busy); then enough slices to
-// give every SM about one item, never more slices than K/V tiles, at most 64.
+// leaves most SMs idle (at most half of them busy); then as many slices as
+// keep all items in one round (items <= SMs: a second, partial round would
+// double the time), never more slices than K/V tiles, at most 64.
 int choose_splits(int64_t BH, int Nq, int Nk, int sms) {
     const int64_t pairs = BH * ((Nq + 2 * fa::kBR - 1) / (2 * fa::kBR));
     if (2 * pairs > sms) return 1;
     const int64_t tc = (Nk + fa::kBC - 1) / fa::kBC;
-    int64_t s = (static_cast<int64_t>(sms) + pairs - 1) / pairs;
+    int64_t s = static_cast<int64_t>(sms) / pairs;
     if (s > tc) s = tc;
     if (s > 64) s = 64;
     return s < 1 ? 1 : static_cast<int>(s);

@@ -15,9 +15,10 @@ Generator (counter-based, so any element can be drawn independently):
   then z_{2i} = r cos(2 pi u2), z_{2i+1} = r sin(2 pi u2), r = sqrt(-2 ln u1).
 * value = sigma * z, rounded to fp32, then to bf16 with round-to-nearest-even.
 
-Workloads: the five attention-forward shapes this library is measured on, plus
-the ragged-tail variant of the short-query shape (Nk = 8192 + 37).  Q, K, V of
-workload number c use seeds 1000*c + 0, 1, 2.
+Workloads: the five attention-forward shapes this library is measured on, the
+ragged-tail variant of the short-query shape (Nk = 8192 + 37), and a decoding
+shape for the split-key path.  Q, K, V of workload number c use seeds
+1000*c + 0, 1, 2.
 """
 from __future__ import annotations
 
@@ -121,6 +122,9 @@ WORKLOADS = {
                  sigma_q=2.0, sigma_k=2.0, sigma_v=1.0),
         Workload("b8_h32_q128_kv8192_d128", 5, 8, 32, 128, 8192, 128, False),
         Workload("b8_h32_q128_kv8229_d128", 5, 8, 32, 128, 8229, 128, False),
+        # decoding: one query per head against a long key/value cache, the case
+        # the split-key path exists for (32 work items without splitting)
+        Workload("decode_b1_h32_q1_kv32768_d128", 6, 1, 32, 1, 32768, 128, False),
     ]
 }
 

@@ -123,8 +123,9 @@ fa_status fa_fwd_splitkv(const void *Q, const void *K, const void *V, void *O, f
  * fa_splitkv_workspace -- workspace bytes fa_fwd_splitkv needs.  *num_splits
  * = 0 asks for the library's choice for the current device: 1 (no
  * splitting) unless the unsplit work list would keep at most half of the SMs
- * busy, else about one work item per SM, at most one slice per 128-key tile
- * and at most 64 (this reads the device's SM count); any other value is used
+ * busy, else the most slices that keep every work item in one round (items
+ * <= SMs), at most one slice per 128-key tile and at most 64 (this reads the
+ * device's SM count); any other value is used
  * as given.  No allocation and no GPU work; with *num_splits > 0 no GPU is
  * needed at all.  With one slice fa_fwd_splitkv is fa_fwd and does not touch
  * the workspace.

@@ -244,7 +244,7 @@ def run_split(ops, q, k, v, scale, causal, splits):
     return o, lse
 
 
-@pytest.mark.parametrize("name", ["b8_h32_q128_kv8192_d128", "b8_h32_q128_kv8229_d128"])
+@pytest.mark.parametrize("name", ["b8_h32_q128_kv8192_d128", "b8_h32_q128_kv8229_d128", "decode_b1_h32_q1_kv32768_d128"])
 def test_split_keys_short_query_long_key_workloads(ops, name):
     w = inputs.WORKLOADS[name]
     q, k, v, scale = inputs.make_inputs(w)
