@@ -22,7 +22,7 @@ import subprocess
 
 import numpy as np
 
-from . import online  # noqa: F401  (re-exported)
+from . import backward, online  # noqa: F401  (re-exported)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
