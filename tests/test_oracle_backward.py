@@ -104,11 +104,11 @@ def test_planted_mistakes_are_caught_by_finite_differences():
             dS = P * dP; dQ, dK = scale * dS @ K, scale * dS.T @ Q
         if variant == "scale dropped in dQ":
             dQ = dS @ K
-        if variant == "P instead of P^T in dV":
-            dV = (P @ np.ones((5, 4)) @ dO)[:5] if P.shape[0] != P.shape[1] else P @ dO
+        if variant == "unnormalised P in dV":
+            dV = np.exp(S - S.max(axis=1, keepdims=True)).T @ dO
         return dQ, dK, dV
 
-    for variant in ["no rowsum term", "scale dropped in dQ", "P instead of P^T in dV"]:
+    for variant in ["no rowsum term", "scale dropped in dQ", "unnormalised P in dV"]:
         g = grads(variant)
         assert max(np.max(np.abs(a - b)) for a, b in zip(g, fd)) > 1e-3, variant
     assert max(np.max(np.abs(a - b)) for a, b in zip(grads("none"), fd)) < 1e-7
