@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/fa.h"
+#include "fa_bwd_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 
 namespace {
@@ -161,6 +162,7 @@ size_t splitkv_bytes(int64_t BH, int Nq, int d, int splits) {
 struct DeviceInfo {
     int sms = 0;
     bool attr64 = false, attr128 = false;
+    bool bwd_attr64 = false, bwd_attr128 = false;
 };
 std::mutex g_dev_mu;
 DeviceInfo g_dev[64];
@@ -386,6 +388,84 @@ extern "C" fa_status fa_fwd_splitkv_noalloc(const void *Q, const void *K, const 
     st = run_forward(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, causal, num_splits, O_part, LSE_part, s);
     if (st != FA_OK) return st;
     return run_merge(O_part, LSE_part, O, LSE, BH * Nq, d, num_splits, s);
+}
+
+// ------------------------------------------------------------------ backward
+
+namespace {
+
+template <int D>
+fa_status launch_bwd(const fa::BwdParams &p, const void *O, const void *dO, float *Dsum, cudaStream_t stream,
+                     bool &attr_done) {
+    using C = fa::BwdConfig<D>;
+    if (!attr_done) {
+        if (cudaFuncSetAttribute(fa::fa_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::kSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(fa::fa_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::kSmemBytes) != cudaSuccess)
+            return FA_ERR_CUDA;
+        attr_done = true;
+    }
+    const long long rows = static_cast<long long>(p.BH) * p.Nq;
+    fa::fa_bwd_dot_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(O), static_cast<const __nv_bfloat16 *>(dO), Dsum, rows);
+    fa::fa_bwd_dkdv_kernel<D><<<static_cast<unsigned>(p.BH) * p.Tc, fa::kBwdThreads, C::kSmemBytes, stream>>>(p);
+    fa::fa_bwd_dq_kernel<D><<<static_cast<unsigned>(p.BH) * p.Tr, fa::kBwdThreads, C::kSmemBytes, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" fa_status fa_bwd_workspace(int B, int H, int Nq, int Nk, int d, size_t *bytes) {
+    if (!bytes) return FA_ERR_INVALID_ARG;
+    char dummy[16] __attribute__((aligned(16)));
+    fa_status st = validate(dummy, dummy, dummy, dummy, reinterpret_cast<float *>(dummy), B, H, Nq, Nk, d, 1.0f);
+    if (st != FA_OK) return st;
+    *bytes = static_cast<size_t>(B) * H * Nq * 4;
+    return FA_OK;
+}
+
+extern "C" fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const float *LSE,
+                            const void *dO, void *dQ, void *dK, void *dV, int B, int H, int Nq, int Nk, int d,
+                            float scale, int causal, void *workspace, size_t workspace_bytes, fa_stream_t stream) {
+    fa_status st = validate(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale);
+    if (st != FA_OK) return st;
+    if (!dO || !dQ || !dK || !dV || !workspace) return FA_ERR_INVALID_ARG;
+    if (!aligned(dO, 16) || !aligned(dQ, 16) || !aligned(dK, 16) || !aligned(dV, 16) || !aligned(workspace, 16))
+        return FA_ERR_MISALIGNED;
+    const int64_t BH = static_cast<int64_t>(B) * H;
+    if (workspace_bytes < static_cast<size_t>(BH) * Nq * 4) return FA_ERR_INVALID_ARG;
+    int sms;
+    bool *attr_fwd;
+    st = device_info(d, sms, attr_fwd);
+    if (st != FA_OK) return st;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    fa::BwdParams p;
+    std::memset(&p, 0, sizeof p);
+    if (!make_map(&p.tmQ, Q, BH, Nq, d) || !make_map(&p.tmK, K, BH, Nk, d) || !make_map(&p.tmV, V, BH, Nk, d) ||
+        !make_map(&p.tmdO, dO, BH, Nq, d))
+        return FA_ERR_CUDA;
+    p.LSE = LSE;
+    p.Dsum = static_cast<float *>(workspace);
+    p.dQ = static_cast<__nv_bfloat16 *>(dQ);
+    p.dK = static_cast<__nv_bfloat16 *>(dK);
+    p.dV = static_cast<__nv_bfloat16 *>(dV);
+    p.BH = static_cast<int>(BH);
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.Tr = (Nq + fa::kBR - 1) / fa::kBR;
+    p.Tc = (Nk + fa::kBC - 1) / fa::kBC;
+    p.causal = causal != 0;
+    p.scale = scale;
+    double c2 = static_cast<double>(scale) * 1.4426950408889634;
+    if (scale == 0.0f) c2 = 1.1754943508222875e-38 * 1.4426950408889634;
+    p.c2 = static_cast<float>(c2);
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    bool &attr = d == 64 ? g_dev[dev].bwd_attr64 : g_dev[dev].bwd_attr128;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return d == 64 ? launch_bwd<64>(p, O, dO, static_cast<float *>(workspace), s, attr)
+                   : launch_bwd<128>(p, O, dO, static_cast<float *>(workspace), s, attr);
 }
 
 extern "C" fa_status fa_check_device_status(fa_stream_t stream) {

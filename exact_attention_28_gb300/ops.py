@@ -46,6 +46,10 @@ def load_library(path: str | None = None):
     lib.fa_fwd_splitkv_noalloc.restype = i
     lib.fa_splitkv_workspace.argtypes = [i, i, i, i, i, i, vp, vp]
     lib.fa_splitkv_workspace.restype = i
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, ctypes.c_size_t, vp]
+    lib.fa_bwd.restype = i
+    lib.fa_bwd_workspace.argtypes = [i, i, i, i, i, vp]
+    lib.fa_bwd_workspace.restype = i
     lib.fa_check_device_status.argtypes = [vp]
     lib.fa_check_device_status.restype = i
     lib.fa_schedule.argtypes = [i, i, i, i, i, i, i, i, vp, ctypes.c_int64, vp]
@@ -108,6 +112,26 @@ def fa_fwd_host(hq, hk, hv, ho, hlse, dq, dk, dv, do, dlse, scale, causal=False,
                                       hlse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                                       do.data_ptr(), dlse.data_ptr(), B, H, Nq, Nk, d, scale,
                                       int(bool(causal)), _stream_handle(stream)))
+
+
+def fa_bwd(q, k, v, o, lse, do, dq=None, dk=None, dv=None, scale=None, causal=False, workspace=None,
+           stream=None):
+    """dQ, dK, dV of the attention forward (o, lse from fa_fwd) for upstream gradient do."""
+    B, H, Nq, Nk, d = _shape(q, k)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    nb = ctypes.c_size_t(0)
+    _check(load_library().fa_bwd_workspace(B, H, Nq, Nk, d, ctypes.byref(nb)))
+    if workspace is None:
+        workspace = torch.empty(nb.value, dtype=torch.uint8, device=q.device)
+    _check(load_library().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                 do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, d,
+                                 scale, int(bool(causal)), workspace.data_ptr(), workspace.numel(),
+                                 _stream_handle(stream)))
+    return dq, dk, dv
 
 
 def check_device_status(stream=None):

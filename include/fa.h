@@ -134,6 +134,33 @@ fa_status fa_splitkv_workspace(int B, int H, int Nq, int Nk, int d, int causal, 
                                size_t *bytes);
 
 /*
+ * fa_bwd -- gradients of the attention forward ("6. FlashAttention 分块逻辑"
+ * section 7; "9.4 FlashAttention 与 FlashMLA" sections 9.4.3 and 9.4.5): P is
+ * recomputed tile by tile from Q, K and the forward's LSE, never stored, and
+ *   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - rowsum(dO * O)),
+ *   dQ = scale dS K,  dK = scale dS^T Q.
+ * Three kernels run on `stream`: rowsum(dO * O) into the workspace, dK/dV
+ * (one CTA per 128-key tile, looping over query tiles) and dQ (one CTA per
+ * 128-query tile, looping over key tiles).
+ *
+ *   Q, K, V, O, LSE  the forward's inputs and outputs (fa_fwd layouts)
+ *   dO    bf16 [B, H, Nq, d]  gradient of the loss with respect to O
+ *   dQ    bf16 [B, H, Nq, d]  output;  dK, dV  bf16 [B, H, Nk, d]  outputs
+ *   workspace  caller-owned device memory, 16-byte aligned, at least
+ *              fa_bwd_workspace bytes (fp32 [B, H, Nq]); contents ignored
+ *   B, H, Nq, Nk, d, scale, causal: exactly those of the forward call
+ * Errors as fa_fwd; FA_ERR_INVALID_ARG also for a NULL dO, dQ, dK, dV or
+ * workspace or a too small workspace.  Outputs must not overlap inputs.
+ */
+fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const float *LSE,
+                 const void *dO, void *dQ, void *dK, void *dV,
+                 int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                 void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* fa_bwd_workspace -- bytes of workspace fa_bwd needs (B * H * Nq * 4). No GPU needed. */
+fa_status fa_bwd_workspace(int B, int H, int Nq, int Nk, int d, size_t *bytes);
+
+/*
  * fa_fwd_splitkv_noalloc -- fa_fwd_splitkv for callers that cannot allocate
  * device memory: code being recorded into a CUDA graph (an allocation is not
  * replayed, and cudaMalloc may synchronise the device), serving loops whose

@@ -1,0 +1,86 @@
+"""GPU parity of the backward (fa_bwd) against the fp64 backward oracle.
+
+Tolerance, derived from the arithmetic (the pages give none for gradients):
+bf16 inputs, P and dS rounded to bf16 (relative 2^-9) before the gradient
+GEMMs, fp32 accumulation, bf16 outputs.  Per gradient G:
+  max |G_gpu - G_ref| <= 2e-2 * max |G_ref| + 1e-4
+  mean |G_gpu - G_ref| <= 1e-2 * mean |G_ref| + 1e-5
+The absolute terms cover gradients that are exactly zero (one visible key:
+dS = P (dP - D) vanishes, up to the rounding of O inside D).
+"""
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+from oracle import backward  # noqa: E402
+from exact_attention_28_gb300 import inputs  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ops():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from exact_attention_28_gb300 import build, ops as _ops
+    build.build()
+    _ops.load_library()
+    return _ops
+
+
+def to_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def check(name, got, ref):
+    got = got.float().cpu().numpy().astype(np.float64)
+    err = np.abs(got - ref)
+    top = np.max(np.abs(ref))
+    assert np.all(np.isfinite(got)), name
+    assert err.max() <= 2e-2 * top + 1e-4, f"{name}: max err {err.max():.3e} vs max |ref| {top:.3e}"
+    assert err.mean() <= 1e-2 * np.mean(np.abs(ref)) + 1e-5, f"{name}: mean err {err.mean():.3e}"
+
+
+def run_case(ops, B, H, Nq, Nk, d, causal, seed=0, scale=None):
+    q, k, v = inputs.custom_inputs(1234 + seed, B, H, Nq, Nk, d)
+    do = inputs.normal_bf16(99 + seed, (B, H, Nq, d))
+    scale = float(np.float32(1 / math.sqrt(d))) if scale is None else scale
+    Q, K, V, dO = to_dev(q), to_dev(k), to_dev(v), to_dev(do)
+    O, L = ops.fa_fwd(Q, K, V, scale=scale, causal=causal)
+    dQ, dK, dV = ops.fa_bwd(Q, K, V, O, L, dO, scale=scale, causal=causal)
+    ops.check_device_status()
+    f = oracle.bf16_bits_to_f64
+    rQ, rK, rV = backward.backward_heads(f(q), f(k), f(v), f(do), float(np.float32(scale)), causal)
+    check("dQ", dQ, rQ)
+    check("dK", dK, rK)
+    check("dV", dV, rV)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq,Nk", [(256, 256), (384, 640), (640, 384), (300, 200), (129, 257), (1, 130), (128, 1)])
+def test_backward_against_oracle(ops, d, causal, Nq, Nk):
+    run_case(ops, 1, 2, Nq, Nk, d, causal, seed=Nq + Nk)
+
+
+def test_backward_many_heads(ops):
+    run_case(ops, 2, 8, 512, 512, 128, True, seed=7)
+
+
+@pytest.mark.parametrize("scale", [0.5, -0.2])
+def test_backward_other_scales(ops, scale):
+    run_case(ops, 1, 2, 200, 300, 64, False, seed=11, scale=scale)
+
+
+def test_backward_zero_upstream_gradient_gives_zero(ops):
+    q, k, v = inputs.custom_inputs(5, 1, 2, 256, 256, 128)
+    Q, K, V = to_dev(q), to_dev(k), to_dev(v)
+    O, L = ops.fa_fwd(Q, K, V, causal=True)
+    dQ, dK, dV = ops.fa_bwd(Q, K, V, O, L, torch.zeros_like(Q), causal=True)
+    ops.check_device_status()
+    for g in (dQ, dK, dV):
+        assert torch.count_nonzero(g).item() == 0
