@@ -282,13 +282,28 @@ def run_ours(args, w):
 
     workspace = None
     splits = 1
+    if args.path == "bwd":
+        # forward outputs and an upstream gradient for every input set
+        import ctypes
+        nb = ctypes.c_size_t(0)
+        ops._check(ops.load_library().fa_bwd_workspace(w.B, w.H, w.Nq, w.Nk, w.d, ctypes.byref(nb)))
+        workspace = torch.empty(nb.value, dtype=torch.uint8, device="cuda")
+        bwd_bufs = []
+        for si, s in enumerate(sets):
+            ops.fa_fwd(s[0], s[1], s[2], s[3], s[4], scale=scale, causal=w.causal, stream=stream)
+            do = as_t(inputs.normal_bf16(7000 + si, (w.B, w.H, w.Nq, w.d))).cuda()
+            bwd_bufs.append((do, torch.empty_like(s[0]), torch.empty_like(s[1]), torch.empty_like(s[2])))
     if args.path == "splitkv":
         splits, nbytes = ops.splitkv_workspace(w.B, w.H, w.Nq, w.Nk, w.d, w.causal, 0)
         workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
 
     def step(i):
         s = sets[i % n_sets]
-        if args.path == "splitkv":
+        if args.path == "bwd":
+            b = bwd_bufs[i % n_sets]
+            ops.fa_bwd(s[0], s[1], s[2], s[3], s[4], b[0], b[1], b[2], b[3], scale=scale, causal=w.causal,
+                       workspace=workspace, stream=stream)
+        elif args.path == "splitkv":
             ops.fa_fwd_splitkv(s[0], s[1], s[2], s[3], s[4], scale=scale, causal=w.causal, num_splits=splits,
                                workspace=workspace, stream=stream)
         else:
@@ -325,18 +340,20 @@ def run_ours(args, w):
 
     # end to end through the host-buffer entry point
     e2e_ms = float("nan")
-    if not args.no_e2e:
+    if not args.no_e2e and args.path == "fwd":
         e2e_ms = run_e2e(args, w, hq, hk, hv, sets[0], scale, stream)
-    if not args.no_e2e:
+    if not args.no_e2e and args.path == "fwd":
         e2e_ms = reduce_max([e2e_ms], world)[0]
     if rank == 0:
         peaks, peak_src = measured_peaks()
         ms_per_step = total_ms / args.steps
-        value = aggregate_tflops(w.flops, ms_per_step, world)
+        # backward: five GEMMs of 2*Nq*Nk*d (dV, dP, dQ, dK and the recomputed S), 2.5x the forward
+        flops = w.flops * 5 // 2 if args.path == "bwd" else w.flops
+        value = aggregate_tflops(flops, ms_per_step, world)
         ridge = float(peaks["bf16_tflops"]) * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
-        tensor_bound = w.flops / w.algorithmic_bytes >= ridge
+        tensor_bound = flops / w.algorithmic_bytes >= ridge
         if tensor_bound:
-            achieved, peak, unit, bound = w.flops / (launch_ms * 1e-3) / 1e12, float(peaks["bf16_tflops"]), \
+            achieved, peak, unit, bound = flops / (launch_ms * 1e-3) / 1e12, float(peaks["bf16_tflops"]), \
                 "TFLOP/s", "tensor"
         else:
             achieved, peak, unit, bound = w.algorithmic_bytes / (launch_ms * 1e-3) / 1e9, float(peaks["hbm_gbs"]), \
@@ -352,14 +369,15 @@ def run_ours(args, w):
                          "peak_source": f"{peak_src} " + ("bf16_tflops (burst)" if tensor_bound else "hbm_gbs"),
                          "frac_of_sustained": (achieved / float(peaks.get("bf16_tflops_sustained", peak))
                                                if tensor_bound else None),
-                         "kernel": "fa_fwd_kernel<%d>" % w.d + (" + fa_merge_kernel" if splits > 1 else ""),
+                         "kernel": ("fa_bwd_dot + fa_bwd_dkdv + fa_bwd_dq <%d>" % w.d if args.path == "bwd" else
+                                    "fa_fwd_kernel<%d>" % w.d + (" + fa_merge_kernel" if splits > 1 else "")),
                          "launch_ms": launch_ms},
-            "e2e": None if args.no_e2e else {
+            "e2e": None if (args.no_e2e or args.path != "fwd") else {
                 "value": aggregate_tflops(w.flops, e2e_ms, world), "unit": "TFLOPS",
                 "h2d_bytes_per_step": 2 * (hq.numel() + 2 * hk.numel()),
                 "d2h_bytes_per_step": 2 * hq.numel() + 4 * w.B * w.H * w.Nq,
                 "ms_per_step": e2e_ms},
-            "gpu_launches": args.steps * (2 if splits > 1 else 1),
+            "gpu_launches": args.steps * (3 if args.path == "bwd" else (2 if splits > 1 else 1)),
             "clocks": sampler.summary(t0, t1) if sampler else None,
         }
         if world == 1 and not args.no_cpu_baseline:
@@ -383,8 +401,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
-    ap.add_argument("--path", choices=["fwd", "splitkv"], default="fwd",
-                    help="fa_fwd, or fa_fwd_splitkv with the library's slice count")
+    ap.add_argument("--path", choices=["fwd", "splitkv", "bwd"], default="fwd",
+                    help="fa_fwd, fa_fwd_splitkv with the library's slice count, or fa_bwd")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
