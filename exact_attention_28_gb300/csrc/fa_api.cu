@@ -51,6 +51,22 @@ bool make_map(CUtensorMap *map, const void *ptr, int64_t BH, int64_t N, int d) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Paged cache [num_blocks][H][block_size][d] bf16, boxes of 64 columns x
+// min(block_size, 128) rows of one head of one block, 128-byte swizzle.
+bool make_map_paged(CUtensorMap *map, const void *ptr, int num_blocks, int H, int block_size, int d) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(block_size),
+                                static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(num_blocks)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(block_size) * d * 2,
+                                   static_cast<cuuint64_t>(H) * block_size * d * 2};
+    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(block_size < fa::kBC ? block_size : fa::kBC), 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 fa_status validate(const void *Q, const void *K, const void *V, const void *O, const float *LSE, int B,
@@ -238,6 +254,43 @@ extern "C" fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O
     if (st != FA_OK) return st;
     return run_forward(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, causal, 1, nullptr, nullptr,
                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" fa_status fa_fwd_paged(const void *Q, const void *K_cache, const void *V_cache, const int *block_table,
+                                  const int *seq_lens, void *O, float *LSE, int B, int H, int Nq, int max_blocks,
+                                  int num_blocks, int block_size, int d, float scale, int causal,
+                                  fa_stream_t stream) {
+    if (!block_table || !seq_lens) return FA_ERR_INVALID_ARG;
+    if (max_blocks < 1 || num_blocks < 1) return FA_ERR_INVALID_ARG;
+    if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128 && block_size != 256)
+        return FA_ERR_UNSUPPORTED;
+    const int64_t cap = static_cast<int64_t>(max_blocks) * block_size;
+    if (cap > (int64_t{1} << 30) || static_cast<int64_t>(num_blocks) * H * block_size * d * 2 >= (int64_t{1} << 40))
+        return FA_ERR_INVALID_ARG;
+    fa_status st = validate(Q, K_cache, V_cache, O, LSE, B, H, Nq, static_cast<int>(cap), d, scale);
+    if (st != FA_OK) return st;
+    if (!aligned(block_table, 4) || !aligned(seq_lens, 4)) return FA_ERR_MISALIGNED;
+    int sms;
+    bool *attr_done;
+    st = device_info(d, sms, attr_done);
+    if (st != FA_OK) return st;
+    fa::FwdParams p;
+    const int grid = setup_params(p, B, H, Nq, static_cast<int>(cap), d, scale, causal, sms, 1);
+    const int64_t BH = static_cast<int64_t>(B) * H;
+    if (!make_map(&p.tmQ, Q, BH, Nq, d) || !make_map_paged(&p.tmK, K_cache, num_blocks, H, block_size, d) ||
+        !make_map_paged(&p.tmV, V_cache, num_blocks, H, block_size, d))
+        return FA_ERR_CUDA;
+    p.O = static_cast<__nv_bfloat16 *>(O);
+    p.LSE = LSE;
+    p.paged = 1;
+    p.H = H;
+    p.block_size = block_size;
+    p.max_blocks = max_blocks;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return d == 64 ? launch<64>(p, grid, s, *attr_done) : launch<128>(p, grid, s, *attr_done);
 }
 
 extern "C" fa_status fa_splitkv_workspace(int B, int H, int Nq, int Nk, int d, int causal, int *num_splits,

@@ -106,6 +106,12 @@ struct FwdParams {
     int kv_splits;     // > 1: each item covers 1/kv_splits of its key range and writes partials
     float *O_part;     // [kv_splits][BH][Nq][D] fp32 partial outputs (normalised by their own sum)
     float *LSE_part;   // [kv_splits][BH][Nq] fp32 partial log-sum-exp (-inf: no visible key)
+    // paged key/value cache (paged != 0): tmK/tmV are 4-D maps over
+    // [num_blocks][H][block_size][D]; key position k of sequence b lives in
+    // row k % block_size of physical block block_table[b][k / block_size]
+    int paged, H, block_size, max_blocks;
+    const int *block_table;   // [B][max_blocks]; < 0: unallocated (its keys are skipped)
+    const int *seq_lens;      // [B] keys per sequence
     int causal;
     float c2;          // scale * log2(e)
 };
@@ -118,6 +124,8 @@ struct Item {
     int nk[2];     // one past the last K/V tile each query tile visits; a tile with
                    // nk <= kv0 has nothing to do in this item
     int split;     // index of the key-range slice (0 without splitting)
+    int seq_len;   // keys of this item's sequence (Nk unless paged)
+    int q_shift;   // causal: query row i sees keys k <= i + q_shift
 };
 
 // Item w of the list.  Heads are taken in groups of heads_per_group whose
@@ -164,6 +172,8 @@ __host__ __device__ __forceinline__ Item decode_item(const FwdParams &p, int w) 
         vis[t] = nk;
     }
     it.split = split;
+    it.seq_len = p.Nk;
+    it.q_shift = 0;
     if (p.kv_splits > 1) {
         const int nkv = vis[0] > vis[1] ? vis[0] : vis[1];
         const int kb = split * nkv / p.kv_splits, ke = (split + 1) * nkv / p.kv_splits;
@@ -176,6 +186,64 @@ __host__ __device__ __forceinline__ Item decode_item(const FwdParams &p, int w) 
         it.nk[1] = vis[1];
     }
     return it;
+}
+
+// Device-side completion of an item for the paged cache: the sequence's own
+// key count (read from device memory) bounds every tile's key range, and the
+// Nq queries are the last Nq positions of the sequence, so under the causal
+// mask row i sees keys k <= i + (seq_len - Nq).  A tile left with no visible
+// key gets nk = 0 (its rows are written as empty).
+__device__ __forceinline__ Item resolve_item(const FwdParams &p, int w) {
+    Item it = decode_item(p, w);
+    if (!p.paged) return it;
+    const int cap = p.max_blocks * p.block_size;
+    int seq = __ldg(p.seq_lens + it.bh / p.H);
+    seq = seq < 0 ? 0 : (seq > cap ? cap : seq);
+    it.seq_len = seq;
+    it.q_shift = seq - p.Nq;
+    #pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        if (t >= it.ntiles) { it.nk[t] = 0; continue; }
+        int vis = seq;
+        if (p.causal) {
+            const int q_end = min(p.Nq, it.q0 + (t + 1) * kBR);
+            vis = min(seq, q_end + it.q_shift);
+        }
+        it.nk[t] = vis > 0 ? (vis + kBC - 1) / kBC : 0;
+    }
+    return it;
+}
+
+// Loads one 128-key tile of the paged cache: 128 / block_size boxes (one per
+// page) or one box inside a larger page.  Unallocated or out-of-range pages
+// are read from block 0 and masked by the softmax.
+__device__ __forceinline__ void tma_load_paged_tile(const FwdParams &p, const CUtensorMap *map, uint32_t dst,
+                                                    uint32_t bar, int bh, int j, int chunks, uint64_t pol) {
+    const int b = bh / p.H, h = bh % p.H;
+    const int rows = p.block_size < kBC ? p.block_size : kBC;
+    for (int s = 0; s * rows < kBC; ++s) {
+        const int key = j * kBC + s * rows;
+        const int lp = key / p.block_size;
+        int phy = lp < p.max_blocks ? __ldg(p.block_table + static_cast<size_t>(b) * p.max_blocks + lp) : 0;
+        if (phy < 0) phy = 0;
+        for (int c = 0; c < chunks; ++c)
+            ptx::tma_load_4d(dst + c * kChunkBytes + s * rows * 128, map, bar, c * 64, key % p.block_size, h, phy, pol);
+    }
+}
+
+// Bit c/g set when the keys c..c+g-1 of tile j of sequence b lie in an
+// unallocated page (g = min(block_size, 128)); 0 for a dense cache.
+__device__ __forceinline__ uint32_t paged_holes(const FwdParams &p, int bh, int j) {
+    if (!p.paged) return 0u;
+    const int b = bh / p.H;
+    const int rows = p.block_size < kBC ? p.block_size : kBC;
+    uint32_t holes = 0;
+    for (int s = 0; s * rows < kBC; ++s) {
+        const int lp = (j * kBC + s * rows) / p.block_size;
+        if (lp < p.max_blocks && __ldg(p.block_table + static_cast<size_t>(b) * p.max_blocks + lp) < 0)
+            holes |= 1u << s;
+    }
+    return holes;
 }
 
 // Item index of round k for CTA b of G (snake order), or -1 when done.
@@ -246,7 +314,7 @@ __device__ void producer_role(const FwdParams &p, const Shared &sh, uint32_t sme
     for (int k = 0;; ++k) {
         const int w = item_of_round(p, k);
         if (w < 0) break;
-        const Item item = decode_item(p, w);
+        const Item item = resolve_item(p, w);
         if (k > 0 && !wait_bar(sh.q_empty, (k - 1) & 1, sh.abort_flag, 0, w, -1)) break;
         ptx::mbar_arrive_expect_tx(sh.q_full, item.ntiles * C::kQTileBytes);
         ++q_arms;
@@ -269,10 +337,15 @@ __device__ void producer_role(const FwdParams &p, const Shared &sh, uint32_t sme
                 const uint32_t full = sh.kv_full0 + 8 * slot;
                 ptx::mbar_arrive_expect_tx(full, C::kKVTileBytes);
                 const CUtensorMap *map = which ? &p.tmV : &p.tmK;
-                #pragma unroll
-                for (int c = 0; c < C::kChunks; ++c)
-                    ptx::tma_load_3d(smem_ring + slot * C::kKVTileBytes + c * kChunkBytes, map, full,
-                                     c * 64, j * kBC, item.bh, pol_kv);
+                if (p.paged) {
+                    tma_load_paged_tile(p, map, smem_ring + slot * C::kKVTileBytes, full, item.bh, j, C::kChunks,
+                                        pol_kv);
+                } else {
+                    #pragma unroll
+                    for (int c = 0; c < C::kChunks; ++c)
+                        ptx::tma_load_3d(smem_ring + slot * C::kKVTileBytes + c * kChunkBytes, map, full,
+                                         c * 64, j * kBC, item.bh, pol_kv);
+                }
                 loads_issued = it + 1;
             }
         }
@@ -326,7 +399,7 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
     for (int k = 0;; ++k) {
         const int w = item_of_round(p, k);
         if (w < 0) break;
-        const Item item = decode_item(p, w);
+        const Item item = resolve_item(p, w);
         const int kv0 = item.kv0;
         const int nk0 = item.nk[0], nk1 = item.nk[1];   // tile t is active for kv0 <= j < nk_t
         const int nkv = max(nk0, nk1);
@@ -483,16 +556,24 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
     for (int k = 0;; ++k) {
         const int w = item_of_round(p, k);
         if (w < 0) break;
-        const Item item = decode_item(p, w);
+        const Item item = resolve_item(p, w);
         if (tile >= item.ntiles) continue;
         const int nk = item.nk[tile];
         const int qg = item.q0 + tile * kBR + row;   // this thread's query row
         const size_t prow = (static_cast<size_t>(item.split) * p.BH + item.bh) * p.Nq + qg;   // partial row
-        if (nk <= item.kv0) {   // no visible key in this slice: an empty partial
-            if (qg < p.Nq) p.LSE_part[prow] = -INFINITY;
+        if (nk <= item.kv0) {   // no visible key for this tile (in this slice): empty rows
+            if (qg < p.Nq) {
+                if (p.kv_splits > 1) {
+                    p.LSE_part[prow] = -INFINITY;
+                } else {
+                    __nv_bfloat16 *orow = p.O + (static_cast<size_t>(item.bh) * p.Nq + qg) * D;
+                    for (int c = 0; c < D; c += 8) __stcs(reinterpret_cast<uint4 *>(orow + c), make_uint4(0, 0, 0, 0));
+                    p.LSE[static_cast<size_t>(item.bh) * p.Nq + qg] = -INFINITY;
+                }
+            }
             continue;
         }
-        const int key_lim = p.causal ? min(p.Nk, qg + 1) : p.Nk;
+        const int key_lim = p.causal ? min(item.seq_len, qg + 1 + item.q_shift) : item.seq_len;
         float m_ref = -INFINITY;   // log2-domain reference maximum
         float l = 0.f;             // sum of p (fp32), for LSE
         float l_rounded = 0.f;     // sum of the bf16 p that P V uses, for O
@@ -504,10 +585,12 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
             uint32_t s[128];
             ptx::tmem_load_128cols(tS, s);
             const int kvalid = key_lim - j * kBC;
-            if (__any_sync(0xffffffffu, kvalid < kBC)) {   // warp-uniform masked path
+            const uint32_t holes = paged_holes(p, item.bh, j);   // warp-uniform
+            if (__any_sync(0xffffffffu, kvalid < kBC) || holes) {   // warp-uniform masked path
+                const int g_shift = p.paged ? 31 - __clz(p.block_size < kBC ? p.block_size : kBC) : 7;
                 #pragma unroll
                 for (int c = 0; c < 128; ++c)
-                    if (c >= kvalid) s[c] = __float_as_uint(mask_val);
+                    if (c >= kvalid || ((holes >> (c >> g_shift)) & 1u)) s[c] = __float_as_uint(mask_val);
             }
             const float mx = row_extreme128(s, pos);
             const float m_tile = kvalid > 0 ? mx * c2 : -INFINITY;
@@ -546,9 +629,10 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
         if (!wait_bar(sh.o_full0 + 8 * tile, o_phase, sh.abort_flag, 2 + tile, w, nk)) return;
         o_phase ^= 1u;
         ptx::tc_fence_after_sync();
-        const float inv_l = 1.f / l_rounded;
+        // a row that saw no key at all (possible only with the paged cache) is empty: O = 0, LSE = -inf
+        const float inv_l = l_rounded > 0.f ? 1.f / l_rounded : 0.f;
         const bool live = qg < p.Nq;
-        const float lse = (m_ref + ptx::lg2(l)) * 0.69314718055994531f;
+        const float lse = l > 0.f ? (m_ref + ptx::lg2(l)) * 0.69314718055994531f : -INFINITY;
         if (p.kv_splits > 1) {
             // partial of this key slice: O / l in fp32 and its LSE
             float *prow_o = p.O_part + prow * D;

@@ -46,6 +46,8 @@ def load_library(path: str | None = None):
     lib.fa_fwd_splitkv_noalloc.restype = i
     lib.fa_splitkv_workspace.argtypes = [i, i, i, i, i, i, vp, vp]
     lib.fa_splitkv_workspace.restype = i
+    lib.fa_fwd_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd_paged.restype = i
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, ctypes.c_size_t, vp]
     lib.fa_bwd.restype = i
     lib.fa_bwd_workspace.argtypes = [i, i, i, i, i, vp]
@@ -112,6 +114,29 @@ def fa_fwd_host(hq, hk, hv, ho, hlse, dq, dk, dv, do, dlse, scale, causal=False,
                                       hlse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                                       do.data_ptr(), dlse.data_ptr(), B, H, Nq, Nk, d, scale,
                                       int(bool(causal)), _stream_handle(stream)))
+
+
+def fa_fwd_paged(q, k_cache, v_cache, block_table, seq_lens, o=None, lse=None, scale=None, causal=False,
+                 stream=None):
+    """Attention over a paged cache: k_cache, v_cache [num_blocks, H, block_size, d] bf16,
+    block_table int32 [B, max_blocks], seq_lens int32 [B] (all CUDA tensors)."""
+    B, H, Nq, d = q.shape
+    num_blocks, Hc, block_size, dc = k_cache.shape
+    if Hc != H or dc != d or v_cache.shape != k_cache.shape:
+        raise ValueError("cache shape mismatch")
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_table and seq_lens must be int32")
+    max_blocks = block_table.shape[1]
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _check(load_library().fa_fwd_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
+                                       seq_lens.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Nq, max_blocks,
+                                       num_blocks, block_size, d, scale, int(bool(causal)), _stream_handle(stream)))
+    return o, lse
 
 
 def fa_bwd(q, k, v, o, lse, do, dq=None, dk=None, dv=None, scale=None, causal=False, workspace=None,

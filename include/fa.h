@@ -134,6 +134,38 @@ fa_status fa_splitkv_workspace(int B, int H, int Nq, int Nk, int d, int causal, 
                                size_t *bytes);
 
 /*
+ * fa_fwd_paged -- attention forward over a paged key/value cache ("6.
+ * FlashAttention 分块逻辑", section 12: the block table maps each logical
+ * block of a sequence to a physical block of the cache, unallocated blocks
+ * are skipped, and the tiles are gathered inside the kernel instead of first
+ * copying a contiguous K/V).
+ *
+ *   Q        bf16 [B, H, Nq, d]: the queries of each sequence; they are the
+ *            LAST Nq positions of the sequence (prefill: Nq = seq_len;
+ *            decoding: Nq = 1)
+ *   K_cache, V_cache  bf16 [num_blocks, H, block_size, d], device memory
+ *   block_table  int32 [B, max_blocks], device memory: physical block of
+ *            logical block l of sequence b; a negative entry is unallocated
+ *            and its keys take no part
+ *   seq_lens int32 [B], device memory: keys of sequence b (key position k is
+ *            row k % block_size of block block_table[b][k / block_size]);
+ *            values are clamped to [0, max_blocks * block_size]
+ *   O, LSE   as fa_fwd.  causal != 0: query i of sequence b sees keys
+ *            k <= i + seq_len[b] - Nq.  A row that sees no key at all
+ *            (seq_len < Nq under causal, or only unallocated blocks) gets
+ *            O = 0 and LSE = -inf.
+ *   block_size in {16, 32, 64, 128, 256}; d in {64, 128}.
+ * Errors as fa_fwd; FA_ERR_INVALID_ARG also for NULL block_table/seq_lens or
+ * max_blocks, num_blocks < 1; FA_ERR_UNSUPPORTED for another block_size;
+ * FA_ERR_MISALIGNED for block_table or seq_lens not 4-byte aligned.
+ * Block-table entries >= num_blocks read as zero keys (the copy engine fills
+ * out-of-range rows with zeros); keep them in range.
+ */
+fa_status fa_fwd_paged(const void *Q, const void *K_cache, const void *V_cache, const int *block_table,
+                       const int *seq_lens, void *O, float *LSE, int B, int H, int Nq, int max_blocks,
+                       int num_blocks, int block_size, int d, float scale, int causal, fa_stream_t stream);
+
+/*
  * fa_bwd -- gradients of the attention forward ("6. FlashAttention 分块逻辑"
  * section 7; "9.4 FlashAttention 与 FlashMLA" sections 9.4.3 and 9.4.5): P is
  * recomputed tile by tile from Q, K and the forward's LSE, never stored, and

@@ -10,6 +10,8 @@ Contents
   (``attention.c``), on the bf16 bits the GPU receives, widened to fp64.
 * ``online`` -- the pages' online-softmax recurrences, blocked attention and the
   partial-result merge, in numpy (``online.py``).
+* ``backward`` -- gradients of attention in fp64 (``backward.py``).
+* ``paged`` -- attention over a paged key/value cache (``paged.py``).
 
 Pinned by ``tests/test_oracle_pins.py``; every function has at least one pin
 that does not re-derive it from itself.
@@ -108,3 +110,6 @@ def bf16_bits_to_f64(a) -> np.ndarray:
     """Exact widening of bf16 bit patterns to fp64 (for numpy-side oracle pieces)."""
     a = _u16(a)
     return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+from . import paged  # noqa: E402,F401  (uses bf16_bits_to_f64 above)
