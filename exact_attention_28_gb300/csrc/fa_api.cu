@@ -177,30 +177,38 @@ size_t splitkv_bytes(int64_t BH, int Nq, int d, int splits) {
 
 struct DeviceInfo {
     int sms = 0;
-    bool attr64 = false, attr128 = false;
+    bool attr[2][3] = {};   // forward kernel [d == 128][mode] has its shared-memory limit set
     bool bwd_attr64 = false, bwd_attr128 = false;
 };
 std::mutex g_dev_mu;
 DeviceInfo g_dev[64];
 
-template <int D>
+template <int D, int MODE>
 fa_status launch(const fa::FwdParams &p, int grid, cudaStream_t stream, bool &attr_done) {
     using C = fa::Config<D>;
     if (!attr_done) {
-        if (cudaFuncSetAttribute(fa::fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(fa::fa_fwd_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kSmemBytes) != cudaSuccess)
             return FA_ERR_CUDA;
         attr_done = true;
     }
-    fa::fa_fwd_kernel<D><<<grid, fa::kThreads, C::kSmemBytes, stream>>>(p);
+    fa::fa_fwd_kernel<D, MODE><<<grid, fa::kThreads, C::kSmemBytes, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// Launches the forward variant for head dimension d and the given mode.
+// Caller holds g_dev_mu (attr points into g_dev).
+template <int MODE>
+fa_status launch_mode(const fa::FwdParams &p, int d, int grid, cudaStream_t stream, bool (&attr)[2][3]) {
+    return d == 64 ? launch<64, MODE>(p, grid, stream, attr[0][MODE])
+                   : launch<128, MODE>(p, grid, stream, attr[1][MODE]);
 }
 
 }  // namespace
 
 namespace {
 
-fa_status device_info(int d, int &sms, bool *&attr_done) {
+fa_status device_info(int &sms, DeviceInfo *&out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_dev_mu);
@@ -208,7 +216,7 @@ fa_status device_info(int d, int &sms, bool *&attr_done) {
     if (info.sms == 0 && cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return FA_ERR_CUDA;
     sms = info.sms;
-    attr_done = d == 64 ? &info.attr64 : &info.attr128;
+    out = &info;
     return FA_OK;
 }
 
@@ -218,8 +226,8 @@ fa_status run_forward(const void *Q, const void *K, const void *V, void *O, floa
                       int Nk, int d, float scale, int causal, int kv_splits, float *O_part, float *LSE_part,
                       cudaStream_t stream) {
     int sms;
-    bool *attr_done;
-    fa_status st = device_info(d, sms, attr_done);
+    DeviceInfo *info;
+    fa_status st = device_info(sms, info);
     if (st != FA_OK) return st;
     fa::FwdParams p;
     const int grid = setup_params(p, B, H, Nq, Nk, d, scale, causal, sms, kv_splits);
@@ -231,7 +239,8 @@ fa_status run_forward(const void *Q, const void *K, const void *V, void *O, floa
     p.O_part = O_part;
     p.LSE_part = LSE_part;
     std::lock_guard<std::mutex> lock(g_dev_mu);
-    return d == 64 ? launch<64>(p, grid, stream, *attr_done) : launch<128>(p, grid, stream, *attr_done);
+    return kv_splits > 1 ? launch_mode<fa::kSplit>(p, d, grid, stream, info->attr)
+                         : launch_mode<fa::kDense>(p, d, grid, stream, info->attr);
 }
 
 fa_status run_merge(const float *O_part, const float *LSE_part, void *O, float *LSE, int64_t rows, int d, int splits,
@@ -271,8 +280,8 @@ extern "C" fa_status fa_fwd_paged(const void *Q, const void *K_cache, const void
     if (st != FA_OK) return st;
     if (!aligned(block_table, 4) || !aligned(seq_lens, 4)) return FA_ERR_MISALIGNED;
     int sms;
-    bool *attr_done;
-    st = device_info(d, sms, attr_done);
+    DeviceInfo *info;
+    st = device_info(sms, info);
     if (st != FA_OK) return st;
     fa::FwdParams p;
     const int grid = setup_params(p, B, H, Nq, static_cast<int>(cap), d, scale, causal, sms, 1);
@@ -282,7 +291,6 @@ extern "C" fa_status fa_fwd_paged(const void *Q, const void *K_cache, const void
         return FA_ERR_CUDA;
     p.O = static_cast<__nv_bfloat16 *>(O);
     p.LSE = LSE;
-    p.paged = 1;
     p.H = H;
     p.block_size = block_size;
     p.max_blocks = max_blocks;
@@ -290,7 +298,7 @@ extern "C" fa_status fa_fwd_paged(const void *Q, const void *K_cache, const void
     p.seq_lens = seq_lens;
     std::lock_guard<std::mutex> lock(g_dev_mu);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return d == 64 ? launch<64>(p, grid, s, *attr_done) : launch<128>(p, grid, s, *attr_done);
+    return launch_mode<fa::kPaged>(p, d, grid, s, info->attr);
 }
 
 extern "C" fa_status fa_splitkv_workspace(int B, int H, int Nq, int Nk, int d, int causal, int *num_splits,
@@ -303,8 +311,8 @@ extern "C" fa_status fa_splitkv_workspace(int B, int H, int Nq, int Nk, int d, i
     const int64_t BH = static_cast<int64_t>(B) * H;
     if (*num_splits == 0) {
         int sms;
-        bool *attr_done;
-        st = device_info(d, sms, attr_done);
+        DeviceInfo *info;
+        st = device_info(sms, info);
         if (st != FA_OK) return st;
         *num_splits = choose_splits(BH, Nq, Nk, sms);
     }
@@ -349,7 +357,7 @@ extern "C" fa_status fa_schedule(int B, int H, int Nq, int Nk, int d, int causal
         for (int k = 0;; ++k) {
             const int w = fa::item_of_round(p, k, b, grid);
             if (w < 0) break;
-            const fa::Item it = fa::decode_item(p, w);
+            const fa::Item it = fa::decode_item(p, w, p.kv_splits > 1);
             int32_t *out = items + 8 * n++;
             out[0] = b; out[1] = k; out[2] = it.bh; out[3] = it.q0; out[4] = it.kv0;
             out[5] = it.nk[0]; out[6] = it.ntiles > 1 ? it.nk[1] : -1; out[7] = it.split;
@@ -423,8 +431,8 @@ extern "C" fa_status fa_fwd_splitkv_noalloc(const void *Q, const void *K, const 
     const int64_t BH = static_cast<int64_t>(B) * H;
     if (num_splits == 0) {
         int sms;
-        bool *attr_done;
-        st = device_info(d, sms, attr_done);
+        DeviceInfo *info;
+        st = device_info(sms, info);
         if (st != FA_OK) return st;
         num_splits = choose_splits(BH, Nq, Nk, sms);
     }
@@ -489,11 +497,9 @@ extern "C" fa_status fa_bwd(const void *Q, const void *K, const void *V, const v
     const int64_t BH = static_cast<int64_t>(B) * H;
     if (workspace_bytes < static_cast<size_t>(BH) * Nq * 4) return FA_ERR_INVALID_ARG;
     int sms;
-    bool *attr_fwd;
-    st = device_info(d, sms, attr_fwd);
+    DeviceInfo *info;
+    st = device_info(sms, info);
     if (st != FA_OK) return st;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
     fa::BwdParams p;
     std::memset(&p, 0, sizeof p);
     if (!make_map(&p.tmQ, Q, BH, Nq, d) || !make_map(&p.tmK, K, BH, Nk, d) || !make_map(&p.tmV, V, BH, Nk, d) ||
@@ -515,7 +521,7 @@ extern "C" fa_status fa_bwd(const void *Q, const void *K, const void *V, const v
     if (scale == 0.0f) c2 = 1.1754943508222875e-38 * 1.4426950408889634;
     p.c2 = static_cast<float>(c2);
     std::lock_guard<std::mutex> lock(g_dev_mu);
-    bool &attr = d == 64 ? g_dev[dev].bwd_attr64 : g_dev[dev].bwd_attr128;
+    bool &attr = d == 64 ? info->bwd_attr64 : info->bwd_attr128;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return d == 64 ? launch_bwd<64>(p, O, dO, static_cast<float *>(workspace), s, attr)
                    : launch_bwd<128>(p, O, dO, static_cast<float *>(workspace), s, attr);

@@ -67,6 +67,13 @@ constexpr int kChunkBytes = 128 * 128;  // one [128 rows x 64 bf16] swizzled TMA
 constexpr float kTau = 8.0f;            // log2-domain slack before the max is raised
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait, then abort
 
+// Kernel variants, fixed at compile time so that the dense forward carries
+// none of the other two's per-tile work:
+//   kDense -- contiguous K/V, one item per (head, query-tile pair), bf16 O;
+//   kSplit -- contiguous K/V, items cut into key-range slices, fp32 partials;
+//   kPaged -- K/V gathered from a block table, per-sequence key counts.
+enum Mode : int { kDense = 0, kSplit = 1, kPaged = 2 };
+
 // Device status word: bit 0 = a pipeline wait expired, bit 1 = a shutdown
 // wait expired.  Read and cleared by the host.
 __device__ unsigned int g_fa_status;
@@ -106,10 +113,10 @@ struct FwdParams {
     int kv_splits;     // > 1: each item covers 1/kv_splits of its key range and writes partials
     float *O_part;     // [kv_splits][BH][Nq][D] fp32 partial outputs (normalised by their own sum)
     float *LSE_part;   // [kv_splits][BH][Nq] fp32 partial log-sum-exp (-inf: no visible key)
-    // paged key/value cache (paged != 0): tmK/tmV are 4-D maps over
+    // paged key/value cache (kPaged kernels): tmK/tmV are 4-D maps over
     // [num_blocks][H][block_size][D]; key position k of sequence b lives in
     // row k % block_size of physical block block_table[b][k / block_size]
-    int paged, H, block_size, max_blocks;
+    int H, block_size, max_blocks;
     const int *block_table;   // [B][max_blocks]; < 0: unallocated (its keys are skipped)
     const int *seq_lens;      // [B] keys per sequence
     int causal;
@@ -135,9 +142,9 @@ struct Item {
 // with it, each pair appears kv_splits times in a row, once per slice of the
 // keys its tiles can see ("6. FlashAttention 分块逻辑" section 11: the key
 // blocks are processed independently and merged afterwards).
-__host__ __device__ __forceinline__ Item decode_item(const FwdParams &p, int w) {
+__host__ __device__ __forceinline__ Item decode_item(const FwdParams &p, int w, bool splitting) {
     int r, first, single, split = 0;
-    if (p.kv_splits > 1) {
+    if (splitting) {
         r = w / p.kv_splits; split = w - r * p.kv_splits; first = 0; single = 0;
     } else if (w < p.n_pair_items) {
         r = w; first = 0; single = 0;
@@ -174,7 +181,7 @@ __host__ __device__ __forceinline__ Item decode_item(const FwdParams &p, int w) 
     it.split = split;
     it.seq_len = p.Nk;
     it.q_shift = 0;
-    if (p.kv_splits > 1) {
+    if (splitting) {
         const int nkv = vis[0] > vis[1] ? vis[0] : vis[1];
         const int kb = split * nkv / p.kv_splits, ke = (split + 1) * nkv / p.kv_splits;
         it.kv0 = kb;
@@ -193,9 +200,10 @@ __host__ __device__ __forceinline__ Item decode_item(const FwdParams &p, int w) 
 // Nq queries are the last Nq positions of the sequence, so under the causal
 // mask row i sees keys k <= i + (seq_len - Nq).  A tile left with no visible
 // key gets nk = 0 (its rows are written as empty).
+template <int MODE>
 __device__ __forceinline__ Item resolve_item(const FwdParams &p, int w) {
-    Item it = decode_item(p, w);
-    if (!p.paged) return it;
+    Item it = decode_item(p, w, MODE == kSplit);
+    if constexpr (MODE != kPaged) return it;
     const int cap = p.max_blocks * p.block_size;
     int seq = __ldg(p.seq_lens + it.bh / p.H);
     seq = seq < 0 ? 0 : (seq > cap ? cap : seq);
@@ -232,9 +240,8 @@ __device__ __forceinline__ void tma_load_paged_tile(const FwdParams &p, const CU
 }
 
 // Bit c/g set when the keys c..c+g-1 of tile j of sequence b lie in an
-// unallocated page (g = min(block_size, 128)); 0 for a dense cache.
+// unallocated page (g = min(block_size, 128)).
 __device__ __forceinline__ uint32_t paged_holes(const FwdParams &p, int bh, int j) {
-    if (!p.paged) return 0u;
     const int b = bh / p.H;
     const int rows = p.block_size < kBC ? p.block_size : kBC;
     uint32_t holes = 0;
@@ -304,7 +311,7 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
 
 // ------------------------------------------------------------ producer warp
 
-template <int D>
+template <int D, int MODE>
 __device__ void producer_role(const FwdParams &p, const Shared &sh, uint32_t smem_q,
                               uint32_t smem_ring, uint32_t &loads_issued, uint32_t &q_arms) {
     using C = Config<D>;
@@ -314,7 +321,7 @@ __device__ void producer_role(const FwdParams &p, const Shared &sh, uint32_t sme
     for (int k = 0;; ++k) {
         const int w = item_of_round(p, k);
         if (w < 0) break;
-        const Item item = resolve_item(p, w);
+        const Item item = resolve_item<MODE>(p, w);
         if (k > 0 && !wait_bar(sh.q_empty, (k - 1) & 1, sh.abort_flag, 0, w, -1)) break;
         ptx::mbar_arrive_expect_tx(sh.q_full, item.ntiles * C::kQTileBytes);
         ++q_arms;
@@ -337,7 +344,7 @@ __device__ void producer_role(const FwdParams &p, const Shared &sh, uint32_t sme
                 const uint32_t full = sh.kv_full0 + 8 * slot;
                 ptx::mbar_arrive_expect_tx(full, C::kKVTileBytes);
                 const CUtensorMap *map = which ? &p.tmV : &p.tmK;
-                if (p.paged) {
+                if constexpr (MODE == kPaged) {
                     tma_load_paged_tile(p, map, smem_ring + slot * C::kKVTileBytes, full, item.bh, j, C::kChunks,
                                         pol_kv);
                 } else {
@@ -387,7 +394,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
                          (accumulate || kk > 0) ? 1u : 0u);
 }
 
-template <int D>
+template <int D, int MODE>
 __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, uint32_t smem_q,
                          uint32_t smem_ring) {
     using C = Config<D>;
@@ -399,7 +406,7 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
     for (int k = 0;; ++k) {
         const int w = item_of_round(p, k);
         if (w < 0) break;
-        const Item item = resolve_item(p, w);
+        const Item item = resolve_item<MODE>(p, w);
         const int kv0 = item.kv0;
         const int nk0 = item.nk[0], nk1 = item.nk[1];   // tile t is active for kv0 <= j < nk_t
         const int nkv = max(nk0, nk1);
@@ -539,7 +546,7 @@ __device__ __forceinline__ void exp_pack_store128(const uint32_t (&s)[128], floa
     sum_rounded = ((r[0] + r[1]) + (r[2] + r[3])) + ((r[4] + r[5]) + (r[6] + r[7]));
 }
 
-template <int D>
+template <int D, int MODE>
 __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem, int tile, int quad, int lane) {
     const int row = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
@@ -556,14 +563,16 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
     for (int k = 0;; ++k) {
         const int w = item_of_round(p, k);
         if (w < 0) break;
-        const Item item = resolve_item(p, w);
+        const Item item = resolve_item<MODE>(p, w);
         if (tile >= item.ntiles) continue;
         const int nk = item.nk[tile];
         const int qg = item.q0 + tile * kBR + row;   // this thread's query row
         const size_t prow = (static_cast<size_t>(item.split) * p.BH + item.bh) * p.Nq + qg;   // partial row
-        if (nk <= item.kv0) {   // no visible key for this tile (in this slice): empty rows
+        // no visible key for this tile (in this slice): empty rows.  Every
+        // dense tile sees key 0, so only the other variants test for it.
+        if (MODE != kDense && nk <= item.kv0) {
             if (qg < p.Nq) {
-                if (p.kv_splits > 1) {
+                if (MODE == kSplit) {
                     p.LSE_part[prow] = -INFINITY;
                 } else {
                     __nv_bfloat16 *orow = p.O + (static_cast<size_t>(item.bh) * p.Nq + qg) * D;
@@ -585,12 +594,20 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
             uint32_t s[128];
             ptx::tmem_load_128cols(tS, s);
             const int kvalid = key_lim - j * kBC;
-            const uint32_t holes = paged_holes(p, item.bh, j);   // warp-uniform
-            if (__any_sync(0xffffffffu, kvalid < kBC) || holes) {   // warp-uniform masked path
-                const int g_shift = p.paged ? 31 - __clz(p.block_size < kBC ? p.block_size : kBC) : 7;
-                #pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    if (c >= kvalid || ((holes >> (c >> g_shift)) & 1u)) s[c] = __float_as_uint(mask_val);
+            if constexpr (MODE == kPaged) {
+                const uint32_t holes = paged_holes(p, item.bh, j);   // warp-uniform
+                if (__any_sync(0xffffffffu, kvalid < kBC) || holes) {   // warp-uniform masked path
+                    const int g_shift = 31 - __clz(p.block_size < kBC ? p.block_size : kBC);
+                    #pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        if (c >= kvalid || ((holes >> (c >> g_shift)) & 1u)) s[c] = __float_as_uint(mask_val);
+                }
+            } else {
+                if (__any_sync(0xffffffffu, kvalid < kBC)) {   // warp-uniform masked path
+                    #pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        if (c >= kvalid) s[c] = __float_as_uint(mask_val);
+                }
             }
             const float mx = row_extreme128(s, pos);
             const float m_tile = kvalid > 0 ? mx * c2 : -INFINITY;
@@ -633,7 +650,7 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
         const float inv_l = l_rounded > 0.f ? 1.f / l_rounded : 0.f;
         const bool live = qg < p.Nq;
         const float lse = l > 0.f ? (m_ref + ptx::lg2(l)) * 0.69314718055994531f : -INFINITY;
-        if (p.kv_splits > 1) {
+        if constexpr (MODE == kSplit) {
             // partial of this key slice: O / l in fp32 and its LSE
             float *prow_o = p.O_part + prow * D;
             #pragma unroll 1
@@ -675,7 +692,7 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
 
 // ------------------------------------------------------------------- kernel
 
-template <int D>
+template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
     using C = Config<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -740,11 +757,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     uint32_t loads_issued = 0, q_arms = 0;
     if (warp < kSoftmaxWarps) {
         ptx::setmaxnreg_inc<kSoftmaxRegs>();
-        softmax_role<D>(p, sh, tmem, warp >> 2, warp & 3, lane);
+        softmax_role<D, MODE>(p, sh, tmem, warp >> 2, warp & 3, lane);
     } else if (warp == kProducerWarp) {
         ptx::setmaxnreg_dec<kOtherRegs>();
         if (lane == 0) {
-            producer_role<D>(p, sh, smem_q, smem_ring, loads_issued, q_arms);
+            producer_role<D, MODE>(p, sh, smem_q, smem_ring, loads_issued, q_arms);
             // Drain: every copy this CTA started must land before it exits.
             const uint32_t first = loads_issued > (uint32_t)C::kSlots ? loads_issued - C::kSlots : 0u;
             for (uint32_t x = first; x < loads_issued; ++x)
@@ -754,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         __syncwarp();
     } else {
         ptx::setmaxnreg_dec<kOtherRegs>();
-        if (warp == kMmaWarp && lane == 0) mma_role<D>(p, sh, tmem, smem_q, smem_ring);
+        if (warp == kMmaWarp && lane == 0) mma_role<D, MODE>(p, sh, tmem, smem_q, smem_ring);
         __syncwarp();
     }
 
