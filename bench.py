@@ -5,6 +5,8 @@
 
 One step = one fa_fwd launch over one batch of the workload (default: the
 non-causal B=2, H=16, N=4096, d=128 forward).  Prints one JSON line.
+--path splitkv | bwd | paged times fa_fwd_splitkv, fa_bwd or fa_fwd_paged
+on the same workload instead.
 
 * value: device-timed TFLOPS (4*B*H*Nq*Nk*d per step, halved when causal),
   inputs resident in HBM, K back-to-back steps bracketed by barrier + sync,
@@ -102,6 +104,28 @@ def shard_heads(num_heads, rank, world):
     base, extra = divmod(num_heads, world)
     start = rank * base + min(rank, extra)
     return start, start + base + (1 if rank < extra else 0)
+
+
+def paged_cache(k, v, block_size, seed):
+    """K, V [B, H, Nk, d] laid out as a paged cache: ([num_blocks, H, block_size, d]
+    K and V caches, int32 block table [B, ceil(Nk / block_size)]).  Every
+    sequence's logical blocks go to a seeded random permutation of the physical
+    blocks (so consecutive key tiles come from scattered pages); the tail of
+    the last block is zero and lies beyond the sequence length."""
+    import torch
+    B, H, Nk, d = k.shape
+    nb = -(-Nk // block_size)
+    perm = torch.from_numpy(np.random.default_rng(seed).permutation(B * nb).astype(np.int64)).to(k.device)
+    caches = []
+    for x in (k, v):
+        padded = torch.zeros((B, H, nb * block_size, d), dtype=x.dtype, device=x.device)
+        padded[:, :, :Nk] = x
+        blocks = padded.view(B, H, nb, block_size, d).permute(0, 2, 1, 3, 4).reshape(B * nb, H, block_size, d)
+        cache = torch.empty_like(blocks)
+        cache[perm] = blocks
+        caches.append(cache)
+    table = perm.view(B, nb).to(torch.int32)
+    return caches[0], caches[1], table
 
 
 def measured_peaks():
@@ -296,6 +320,17 @@ def run_ours(args, w):
     if args.path == "splitkv":
         splits, nbytes = ops.splitkv_workspace(w.B, w.H, w.Nq, w.Nk, w.d, w.causal, 0)
         workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    if args.path == "paged":
+        # each input set's K/V as a paged cache (same keys, scattered pages)
+        seq_lens = torch.full((w.B,), w.Nk, dtype=torch.int32, device="cuda")
+        paged_bufs = [paged_cache(s[1], s[2], args.block_size, 9000 + si) for si, s in enumerate(sets)]
+        sets = [(s[0], None, None, s[3], s[4]) for s in sets]   # the contiguous K/V are not used
+        torch.cuda.empty_cache()
+        # key slices as the library would choose them for this shape (1: no split, no merge)
+        cap = paged_bufs[0][2].shape[1] * args.block_size
+        splits, nbytes = ops.splitkv_workspace(w.B, w.H, w.Nq, cap, w.d, w.causal, 0)
+        if splits > 1:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
 
     def step(i):
         s = sets[i % n_sets]
@@ -303,6 +338,10 @@ def run_ours(args, w):
             b = bwd_bufs[i % n_sets]
             ops.fa_bwd(s[0], s[1], s[2], s[3], s[4], b[0], b[1], b[2], b[3], scale=scale, causal=w.causal,
                        workspace=workspace, stream=stream)
+        elif args.path == "paged":
+            kc, vc, table = paged_bufs[i % n_sets]
+            ops.fa_fwd_paged(s[0], kc, vc, table, seq_lens, s[3], s[4], scale=scale, causal=w.causal, stream=stream,
+                             num_splits=splits if splits > 1 else None, workspace=workspace)
         elif args.path == "splitkv":
             ops.fa_fwd_splitkv(s[0], s[1], s[2], s[3], s[4], scale=scale, causal=w.causal, num_splits=splits,
                                workspace=workspace, stream=stream)
@@ -363,14 +402,16 @@ def run_ours(args, w):
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0, sigma^2) rounded to bf16)",
-            "config": dict(workload_config(w, l2_note, args), kv_splits=splits),
+            "config": dict(workload_config(w, l2_note, args), kv_splits=splits,
+                           **({"block_size": args.block_size} if args.path == "paged" else {})),
             "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"{peak_src} " + ("bf16_tflops (burst)" if tensor_bound else "hbm_gbs"),
                          "frac_of_sustained": (achieved / float(peaks.get("bf16_tflops_sustained", peak))
                                                if tensor_bound else None),
                          "kernel": ("fa_bwd_dot + fa_bwd_dkdv + fa_bwd_dq <%d>" % w.d if args.path == "bwd" else
-                                    "fa_fwd_kernel<%d>" % w.d + (" + fa_merge_kernel" if splits > 1 else "")),
+                                    "fa_fwd_kernel<%d, %d>" % (w.d, (2 if args.path == "paged" else 0) + (1 if splits > 1 else 0))
+                                    + (" + fa_merge_kernel" if splits > 1 else "")),
                          "launch_ms": launch_ms},
             "e2e": None if (args.no_e2e or args.path != "fwd") else {
                 "value": aggregate_tflops(w.flops, e2e_ms, world), "unit": "TFLOPS",
@@ -401,8 +442,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
-    ap.add_argument("--path", choices=["fwd", "splitkv", "bwd"], default="fwd",
-                    help="fa_fwd, fa_fwd_splitkv with the library's slice count, or fa_bwd")
+    ap.add_argument("--block-size", type=int, default=64, help="page size of --path paged")
+    ap.add_argument("--path", choices=["fwd", "splitkv", "bwd", "paged"], default="fwd",
+                    help="fa_fwd, fa_fwd_splitkv with the library's slice count, fa_bwd, or "
+                         "fa_fwd_paged over the workload's K/V scattered into pages")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

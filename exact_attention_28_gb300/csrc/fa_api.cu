@@ -177,7 +177,7 @@ size_t splitkv_bytes(int64_t BH, int Nq, int d, int splits) {
 
 struct DeviceInfo {
     int sms = 0;
-    bool attr[2][3] = {};   // forward kernel [d == 128][mode] has its shared-memory limit set
+    bool attr[2][4] = {};   // forward kernel [d == 128][mode] has its shared-memory limit set
     bool bwd_attr64 = false, bwd_attr128 = false;
 };
 std::mutex g_dev_mu;
@@ -199,7 +199,7 @@ fa_status launch(const fa::FwdParams &p, int grid, cudaStream_t stream, bool &at
 // Launches the forward variant for head dimension d and the given mode.
 // Caller holds g_dev_mu (attr points into g_dev).
 template <int MODE>
-fa_status launch_mode(const fa::FwdParams &p, int d, int grid, cudaStream_t stream, bool (&attr)[2][3]) {
+fa_status launch_mode(const fa::FwdParams &p, int d, int grid, cudaStream_t stream, bool (&attr)[2][4]) {
     return d == 64 ? launch<64, MODE>(p, grid, stream, attr[0][MODE])
                    : launch<128, MODE>(p, grid, stream, attr[1][MODE]);
 }
@@ -265,10 +265,12 @@ extern "C" fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
-extern "C" fa_status fa_fwd_paged(const void *Q, const void *K_cache, const void *V_cache, const int *block_table,
-                                  const int *seq_lens, void *O, float *LSE, int B, int H, int Nq, int max_blocks,
-                                  int num_blocks, int block_size, int d, float scale, int causal,
-                                  fa_stream_t stream) {
+namespace {
+
+// Arguments of the paged entry points (before anything is enqueued).
+fa_status validate_paged(const void *Q, const void *K_cache, const void *V_cache, const int *block_table,
+                         const int *seq_lens, const void *O, const float *LSE, int B, int H, int Nq, int max_blocks,
+                         int num_blocks, int block_size, int d, float scale) {
     if (!block_table || !seq_lens) return FA_ERR_INVALID_ARG;
     if (max_blocks < 1 || num_blocks < 1) return FA_ERR_INVALID_ARG;
     if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128 && block_size != 256)
@@ -279,26 +281,50 @@ extern "C" fa_status fa_fwd_paged(const void *Q, const void *K_cache, const void
     fa_status st = validate(Q, K_cache, V_cache, O, LSE, B, H, Nq, static_cast<int>(cap), d, scale);
     if (st != FA_OK) return st;
     if (!aligned(block_table, 4) || !aligned(seq_lens, 4)) return FA_ERR_MISALIGNED;
+    return FA_OK;
+}
+
+// Encodes the maps and launches the paged kernel (partials when kv_splits > 1).
+fa_status run_paged(const void *Q, const void *K_cache, const void *V_cache, const int *block_table,
+                    const int *seq_lens, void *O, float *LSE, int B, int H, int Nq, int max_blocks, int num_blocks,
+                    int block_size, int d, float scale, int causal, int kv_splits, float *O_part, float *LSE_part,
+                    cudaStream_t stream) {
+    const int64_t cap = static_cast<int64_t>(max_blocks) * block_size;
     int sms;
     DeviceInfo *info;
-    st = device_info(sms, info);
+    fa_status st = device_info(sms, info);
     if (st != FA_OK) return st;
     fa::FwdParams p;
-    const int grid = setup_params(p, B, H, Nq, static_cast<int>(cap), d, scale, causal, sms, 1);
+    const int grid = setup_params(p, B, H, Nq, static_cast<int>(cap), d, scale, causal, sms, kv_splits);
     const int64_t BH = static_cast<int64_t>(B) * H;
     if (!make_map(&p.tmQ, Q, BH, Nq, d) || !make_map_paged(&p.tmK, K_cache, num_blocks, H, block_size, d) ||
         !make_map_paged(&p.tmV, V_cache, num_blocks, H, block_size, d))
         return FA_ERR_CUDA;
     p.O = static_cast<__nv_bfloat16 *>(O);
     p.LSE = LSE;
+    p.O_part = O_part;
+    p.LSE_part = LSE_part;
     p.H = H;
     p.block_size = block_size;
     p.max_blocks = max_blocks;
     p.block_table = block_table;
     p.seq_lens = seq_lens;
     std::lock_guard<std::mutex> lock(g_dev_mu);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return launch_mode<fa::kPaged>(p, d, grid, s, info->attr);
+    return kv_splits > 1 ? launch_mode<fa::kPagedSplit>(p, d, grid, stream, info->attr)
+                         : launch_mode<fa::kPaged>(p, d, grid, stream, info->attr);
+}
+
+}  // namespace
+
+extern "C" fa_status fa_fwd_paged(const void *Q, const void *K_cache, const void *V_cache, const int *block_table,
+                                  const int *seq_lens, void *O, float *LSE, int B, int H, int Nq, int max_blocks,
+                                  int num_blocks, int block_size, int d, float scale, int causal,
+                                  fa_stream_t stream) {
+    fa_status st = validate_paged(Q, K_cache, V_cache, block_table, seq_lens, O, LSE, B, H, Nq, max_blocks,
+                                  num_blocks, block_size, d, scale);
+    if (st != FA_OK) return st;
+    return run_paged(Q, K_cache, V_cache, block_table, seq_lens, O, LSE, B, H, Nq, max_blocks, num_blocks,
+                     block_size, d, scale, causal, 1, nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" fa_status fa_splitkv_workspace(int B, int H, int Nq, int Nk, int d, int causal, int *num_splits,
@@ -336,6 +362,30 @@ extern "C" fa_status fa_fwd_splitkv(const void *Q, const void *K, const void *V,
     if (num_splits == 1)   // one slice: the plain forward writes O and LSE itself
         return run_forward(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, causal, 1, nullptr, nullptr, s);
     st = run_forward(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, causal, num_splits, O_part, LSE_part, s);
+    if (st != FA_OK) return st;
+    return run_merge(O_part, LSE_part, O, LSE, BH * Nq, d, num_splits, s);
+}
+
+extern "C" fa_status fa_fwd_paged_splitkv(const void *Q, const void *K_cache, const void *V_cache,
+                                          const int *block_table, const int *seq_lens, void *O, float *LSE, int B,
+                                          int H, int Nq, int max_blocks, int num_blocks, int block_size, int d,
+                                          float scale, int causal, int num_splits, void *workspace,
+                                          size_t workspace_bytes, fa_stream_t stream) {
+    fa_status st = validate_paged(Q, K_cache, V_cache, block_table, seq_lens, O, LSE, B, H, Nq, max_blocks,
+                                  num_blocks, block_size, d, scale);
+    if (st != FA_OK) return st;
+    if (num_splits < 1 || num_splits > 256 || !workspace) return FA_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return FA_ERR_MISALIGNED;
+    const int64_t BH = static_cast<int64_t>(B) * H;
+    if (workspace_bytes < splitkv_bytes(BH, Nq, d, num_splits)) return FA_ERR_INVALID_ARG;
+    float *O_part = static_cast<float *>(workspace);
+    float *LSE_part = reinterpret_cast<float *>(static_cast<char *>(workspace) + splitkv_o_bytes(BH, Nq, d, num_splits));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (num_splits == 1)
+        return run_paged(Q, K_cache, V_cache, block_table, seq_lens, O, LSE, B, H, Nq, max_blocks, num_blocks,
+                         block_size, d, scale, causal, 1, nullptr, nullptr, s);
+    st = run_paged(Q, K_cache, V_cache, block_table, seq_lens, O, LSE, B, H, Nq, max_blocks, num_blocks, block_size,
+                   d, scale, causal, num_splits, O_part, LSE_part, s);
     if (st != FA_OK) return st;
     return run_merge(O_part, LSE_part, O, LSE, BH * Nq, d, num_splits, s);
 }

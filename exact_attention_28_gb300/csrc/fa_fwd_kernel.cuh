@@ -68,11 +68,11 @@ constexpr float kTau = 8.0f;            // log2-domain slack before the max is r
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait, then abort
 
 // Kernel variants, fixed at compile time so that the dense forward carries
-// none of the other two's per-tile work:
-//   kDense -- contiguous K/V, one item per (head, query-tile pair), bf16 O;
-//   kSplit -- contiguous K/V, items cut into key-range slices, fp32 partials;
+// none of the others' per-tile work.  Two independent bits:
+//   kSplit -- items cut into key-range slices, fp32 partials (merged afterwards);
 //   kPaged -- K/V gathered from a block table, per-sequence key counts.
-enum Mode : int { kDense = 0, kSplit = 1, kPaged = 2 };
+// kDense (neither) reads contiguous K/V and writes bf16 O directly.
+enum Mode : int { kDense = 0, kSplit = 1, kPaged = 2, kPagedSplit = 3 };
 
 // Device status word: bit 0 = a pipeline wait expired, bit 1 = a shutdown
 // wait expired.  Read and cleared by the host.
@@ -198,59 +198,73 @@ __host__ __device__ __forceinline__ Item decode_item(const FwdParams &p, int w, 
 // Device-side completion of an item for the paged cache: the sequence's own
 // key count (read from device memory) bounds every tile's key range, and the
 // Nq queries are the last Nq positions of the sequence, so under the causal
-// mask row i sees keys k <= i + (seq_len - Nq).  A tile left with no visible
-// key gets nk = 0 (its rows are written as empty).
+// mask row i sees keys k <= i + (seq_len - Nq).  With key splitting the
+// slices divide this per-sequence range.  A tile left with no visible key
+// gets nk <= kv0 (its rows are written as empty).
 template <int MODE>
 __device__ __forceinline__ Item resolve_item(const FwdParams &p, int w) {
-    Item it = decode_item(p, w, MODE == kSplit);
-    if constexpr (MODE != kPaged) return it;
-    const int cap = p.max_blocks * p.block_size;
-    int seq = __ldg(p.seq_lens + it.bh / p.H);
-    seq = seq < 0 ? 0 : (seq > cap ? cap : seq);
-    it.seq_len = seq;
-    it.q_shift = seq - p.Nq;
-    #pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        if (t >= it.ntiles) { it.nk[t] = 0; continue; }
-        int vis = seq;
-        if (p.causal) {
-            const int q_end = min(p.Nq, it.q0 + (t + 1) * kBR);
-            vis = min(seq, q_end + it.q_shift);
+    Item it = decode_item(p, w, (MODE & kSplit) != 0);
+    if constexpr ((MODE & kPaged) == 0) {
+        return it;
+    } else {
+        const int cap = p.max_blocks * p.block_size;
+        int seq = __ldg(p.seq_lens + it.bh / p.H);
+        seq = seq < 0 ? 0 : (seq > cap ? cap : seq);
+        it.seq_len = seq;
+        it.q_shift = seq - p.Nq;
+        int vis[2];
+        #pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            int keys = t < it.ntiles ? seq : 0;
+            if (p.causal && t < it.ntiles) {
+                const int q_end = min(p.Nq, it.q0 + (t + 1) * kBR);
+                keys = min(seq, q_end + it.q_shift);
+            }
+            vis[t] = keys > 0 ? (keys + kBC - 1) / kBC : 0;
         }
-        it.nk[t] = vis > 0 ? (vis + kBC - 1) / kBC : 0;
+        if constexpr ((MODE & kSplit) != 0) {
+            const int nkv = max(vis[0], vis[1]);
+            const int kb = it.split * nkv / p.kv_splits, ke = (it.split + 1) * nkv / p.kv_splits;
+            it.kv0 = kb;
+            #pragma unroll
+            for (int t = 0; t < 2; ++t) it.nk[t] = min(vis[t], ke);
+        } else {
+            it.kv0 = 0;
+            it.nk[0] = vis[0];
+            it.nk[1] = vis[1];
+        }
+        return it;
     }
-    return it;
 }
 
-// Loads one 128-key tile of the paged cache: 128 / block_size boxes (one per
-// page) or one box inside a larger page.  Unallocated or out-of-range pages
-// are read from block 0 and masked by the softmax.
+// Paged cache: a 128-key tile is read as kBC / rows boxes of rows =
+// min(block_size, 128) keys, box s from one page.  page_of_box gives that
+// page for tile j of sequence b, or -1 when it is unallocated or past the
+// table (keys past the table lie beyond the sequence and are masked anyway).
+__device__ __forceinline__ int page_of_box(const FwdParams &p, int b, int j, int s, int rows) {
+    const int lp = (j * kBC + s * rows) / p.block_size;
+    return lp < p.max_blocks ? __ldg(p.block_table + static_cast<size_t>(b) * p.max_blocks + lp) : -1;
+}
+
+// The pages of all boxes of tile j (at most 8: block_size >= 16).
+__device__ __forceinline__ void pages_of_tile(const FwdParams &p, int b, int j, int rows, int (&pg)[8]) {
+    #pragma unroll
+    for (int s = 0; s < 8; ++s) pg[s] = s * rows < kBC ? page_of_box(p, b, j, s, rows) : 0;
+}
+
+// Loads one 128-key tile of the paged cache from the pages pg.  An
+// unallocated page is read from block 0 (its keys are masked by the softmax).
 __device__ __forceinline__ void tma_load_paged_tile(const FwdParams &p, const CUtensorMap *map, uint32_t dst,
-                                                    uint32_t bar, int bh, int j, int chunks, uint64_t pol) {
-    const int b = bh / p.H, h = bh % p.H;
-    const int rows = p.block_size < kBC ? p.block_size : kBC;
-    for (int s = 0; s * rows < kBC; ++s) {
-        const int key = j * kBC + s * rows;
-        const int lp = key / p.block_size;
-        int phy = lp < p.max_blocks ? __ldg(p.block_table + static_cast<size_t>(b) * p.max_blocks + lp) : 0;
-        if (phy < 0) phy = 0;
+                                                    uint32_t bar, int h, int j, int rows, const int (&pg)[8],
+                                                    int chunks, uint64_t pol) {
+    #pragma unroll
+    for (int s = 0; s < 8; ++s) {
+        if (s * rows >= kBC) break;
+        const int phy = pg[s] < 0 ? 0 : pg[s];
+        const int row0 = (j * kBC + s * rows) % p.block_size;
         for (int c = 0; c < chunks; ++c)
-            ptx::tma_load_4d(dst + c * kChunkBytes + s * rows * 128, map, bar, c * 64, key % p.block_size, h, phy, pol);
+            ptx::tma_load_4d(dst + c * kChunkBytes + s * rows * 128, map, bar, c * 64, row0, h, phy, pol);
     }
-}
-
-// Bit c/g set when the keys c..c+g-1 of tile j of sequence b lie in an
-// unallocated page (g = min(block_size, 128)).
-__device__ __forceinline__ uint32_t paged_holes(const FwdParams &p, int bh, int j) {
-    const int b = bh / p.H;
-    const int rows = p.block_size < kBC ? p.block_size : kBC;
-    uint32_t holes = 0;
-    for (int s = 0; s * rows < kBC; ++s) {
-        const int lp = (j * kBC + s * rows) / p.block_size;
-        if (lp < p.max_blocks && __ldg(p.block_table + static_cast<size_t>(b) * p.max_blocks + lp) < 0)
-            holes |= 1u << s;
-    }
-    return holes;
 }
 
 // Item index of round k for CTA b of G (snake order), or -1 when done.
@@ -331,8 +345,19 @@ __device__ void producer_role(const FwdParams &p, const Shared &sh, uint32_t sme
                 ptx::tma_load_3d(smem_q + t * C::kQTileBytes + c * kChunkBytes, &p.tmQ, sh.q_full,
                                  c * 64, item.q0 + t * kBR, item.bh, pol_q);
         const int nkv = max(item.nk[0], item.nk[1]);
+        // paged: the pages of tile j (pg) and of tile j + 1 (pg_next, fetched
+        // one tile ahead so the table lookups do not delay the copies)
+        [[maybe_unused]] int pg[8], pg_next[8];
+        [[maybe_unused]] const int rows = p.block_size < kBC ? p.block_size : kBC;
+        if constexpr ((MODE & kPaged) != 0)
+            if (item.kv0 < nkv) pages_of_tile(p, item.bh / p.H, item.kv0, rows, pg_next);
         bool ok = true;
         for (int j = item.kv0; j < nkv && ok; ++j) {
+            if constexpr ((MODE & kPaged) != 0) {
+                #pragma unroll
+                for (int s = 0; s < 8; ++s) pg[s] = pg_next[s];
+                if (j + 1 < nkv) pages_of_tile(p, item.bh / p.H, j + 1, rows, pg_next);
+            }
             #pragma unroll 1
             for (int which = 0; which < 2; ++which, ++it) {
                 const uint32_t slot = it % C::kSlots;
@@ -344,9 +369,9 @@ __device__ void producer_role(const FwdParams &p, const Shared &sh, uint32_t sme
                 const uint32_t full = sh.kv_full0 + 8 * slot;
                 ptx::mbar_arrive_expect_tx(full, C::kKVTileBytes);
                 const CUtensorMap *map = which ? &p.tmV : &p.tmK;
-                if constexpr (MODE == kPaged) {
-                    tma_load_paged_tile(p, map, smem_ring + slot * C::kKVTileBytes, full, item.bh, j, C::kChunks,
-                                        pol_kv);
+                if constexpr ((MODE & kPaged) != 0) {
+                    tma_load_paged_tile(p, map, smem_ring + slot * C::kKVTileBytes, full, item.bh % p.H, j, rows, pg,
+                                        C::kChunks, pol_kv);
                 } else {
                     #pragma unroll
                     for (int c = 0; c < C::kChunks; ++c)
@@ -558,6 +583,9 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
     // -inf for a positive scale, +inf for a negative one (the host never
     // passes c2 == 0, see fa_fwd).
     const float mask_val = pos ? -INFINITY : INFINITY;
+    // paged: keys per box (min(block_size, 128)) and its log2
+    [[maybe_unused]] const int page_rows = p.block_size < kBC ? p.block_size : kBC;
+    [[maybe_unused]] const int page_shift = (MODE & kPaged) != 0 ? 31 - __clz(page_rows) : 0;
     uint32_t s_phase = 0, o_phase = 0;
 
     for (int k = 0;; ++k) {
@@ -572,7 +600,7 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
         // dense tile sees key 0, so only the other variants test for it.
         if (MODE != kDense && nk <= item.kv0) {
             if (qg < p.Nq) {
-                if (MODE == kSplit) {
+                if ((MODE & kSplit) != 0) {
                     p.LSE_part[prow] = -INFINITY;
                 } else {
                     __nv_bfloat16 *orow = p.O + (static_cast<size_t>(item.bh) * p.Nq + qg) * D;
@@ -588,19 +616,31 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
         float l_rounded = 0.f;     // sum of the bf16 p that P V uses, for O
 
         for (int j = item.kv0; j < nk; ++j) {
+            // paged: lane s looks up the page of box s of this tile before the
+            // wait, so the load overlaps it
+            [[maybe_unused]] int box_page = 0;
+            if constexpr ((MODE & kPaged) != 0)
+                if (lane * page_rows < kBC) box_page = page_of_box(p, item.bh / p.H, j, lane, page_rows);
             if (!wait_bar(sh.s_full0 + 8 * tile, s_phase, sh.abort_flag, 2 + tile, w, j)) return;
             s_phase ^= 1u;
             ptx::tc_fence_after_sync();
             uint32_t s[128];
             ptx::tmem_load_128cols(tS, s);
             const int kvalid = key_lim - j * kBC;
-            if constexpr (MODE == kPaged) {
-                const uint32_t holes = paged_holes(p, item.bh, j);   // warp-uniform
+            if constexpr ((MODE & kPaged) != 0) {
+                // bit s: box s lies in an unallocated page (warp-uniform)
+                const uint32_t holes = __ballot_sync(0xffffffffu, box_page < 0);
                 if (__any_sync(0xffffffffu, kvalid < kBC) || holes) {   // warp-uniform masked path
-                    const int g_shift = 31 - __clz(p.block_size < kBC ? p.block_size : kBC);
+                    // column mask, bit c % 32 of word c / 32 (a box holds >= 16 columns)
+                    uint32_t cm[4];
+                    #pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        cm[q] = ((holes >> ((32 * q) >> page_shift)) & 1u) ? 0x0000FFFFu : 0u;
+                        cm[q] |= ((holes >> ((32 * q + 16) >> page_shift)) & 1u) ? 0xFFFF0000u : 0u;
+                    }
                     #pragma unroll
                     for (int c = 0; c < 128; ++c)
-                        if (c >= kvalid || ((holes >> (c >> g_shift)) & 1u)) s[c] = __float_as_uint(mask_val);
+                        if (c >= kvalid || ((cm[c >> 5] >> (c & 31)) & 1u)) s[c] = __float_as_uint(mask_val);
                 }
             } else {
                 if (__any_sync(0xffffffffu, kvalid < kBC)) {   // warp-uniform masked path
@@ -650,7 +690,7 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
         const float inv_l = l_rounded > 0.f ? 1.f / l_rounded : 0.f;
         const bool live = qg < p.Nq;
         const float lse = l > 0.f ? (m_ref + ptx::lg2(l)) * 0.69314718055994531f : -INFINITY;
-        if constexpr (MODE == kSplit) {
+        if constexpr ((MODE & kSplit) != 0) {
             // partial of this key slice: O / l in fp32 and its LSE
             float *prow_o = p.O_part + prow * D;
             #pragma unroll 1
@@ -822,7 +862,8 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const float *__restrict__
         #pragma unroll
         for (int c = 0; c < D / 32; ++c) acc[c] = fmaf(w, src[lane + 32 * c], acc[c]);
     }
-    const float inv = 1.f / wsum;
+    // a row no slice saw a key of (possible only with the paged cache): O = 0, LSE = -inf
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     __nv_bfloat16 *dst = O + row * D;
     #pragma unroll
     for (int c = 0; c < D / 32; ++c) dst[lane + 32 * c] = __float2bfloat16_rn(acc[c] * inv);

@@ -48,6 +48,9 @@ def load_library(path: str | None = None):
     lib.fa_splitkv_workspace.restype = i
     lib.fa_fwd_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
     lib.fa_fwd_paged.restype = i
+    lib.fa_fwd_paged_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, vp,
+                                         ctypes.c_size_t, vp]
+    lib.fa_fwd_paged_splitkv.restype = i
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, ctypes.c_size_t, vp]
     lib.fa_bwd.restype = i
     lib.fa_bwd_workspace.argtypes = [i, i, i, i, i, vp]
@@ -117,9 +120,13 @@ def fa_fwd_host(hq, hk, hv, ho, hlse, dq, dk, dv, do, dlse, scale, causal=False,
 
 
 def fa_fwd_paged(q, k_cache, v_cache, block_table, seq_lens, o=None, lse=None, scale=None, causal=False,
-                 stream=None):
+                 stream=None, num_splits=None, workspace=None):
     """Attention over a paged cache: k_cache, v_cache [num_blocks, H, block_size, d] bf16,
-    block_table int32 [B, max_blocks], seq_lens int32 [B] (all CUDA tensors)."""
+    block_table int32 [B, max_blocks], seq_lens int32 [B] (all CUDA tensors).
+
+    num_splits: None runs fa_fwd_paged; an int (0 = the library's choice)
+    runs fa_fwd_paged_splitkv with that many key slices, allocating the
+    workspace unless one is given."""
     B, H, Nq, d = q.shape
     num_blocks, Hc, block_size, dc = k_cache.shape
     if Hc != H or dc != d or v_cache.shape != k_cache.shape:
@@ -133,9 +140,20 @@ def fa_fwd_paged(q, k_cache, v_cache, block_table, seq_lens, o=None, lse=None, s
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    _check(load_library().fa_fwd_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
-                                       seq_lens.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Nq, max_blocks,
-                                       num_blocks, block_size, d, scale, int(bool(causal)), _stream_handle(stream)))
+    if num_splits is None:
+        _check(load_library().fa_fwd_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                           block_table.data_ptr(), seq_lens.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                           B, H, Nq, max_blocks, num_blocks, block_size, d, scale,
+                                           int(bool(causal)), _stream_handle(stream)))
+        return o, lse
+    splits, nbytes = splitkv_workspace(B, H, Nq, max_blocks * block_size, d, causal, num_splits)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    _check(load_library().fa_fwd_paged_splitkv(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                               block_table.data_ptr(), seq_lens.data_ptr(), o.data_ptr(),
+                                               lse.data_ptr(), B, H, Nq, max_blocks, num_blocks, block_size, d,
+                                               scale, int(bool(causal)), splits, workspace.data_ptr(),
+                                               workspace.numel() * workspace.element_size(), _stream_handle(stream)))
     return o, lse
 
 

@@ -166,6 +166,26 @@ fa_status fa_fwd_paged(const void *Q, const void *K_cache, const void *V_cache, 
                        int num_blocks, int block_size, int d, float scale, int causal, fa_stream_t stream);
 
 /*
+ * fa_fwd_paged_splitkv -- fa_fwd_paged with each query tile's key range cut
+ * into num_splits slices run as independent work items and merged afterwards
+ * (the decoding case of "6. FlashAttention 分块逻辑": section 12's paged
+ * cache read in parallel slices as in section 11, merged as in section 13.2).
+ * The slices divide each sequence's own visible key range, so short
+ * sequences get short slices; a slice with no key contributes nothing.
+ *
+ *   Q .. causal  as fa_fwd_paged
+ *   num_splits, workspace, workspace_bytes  as fa_fwd_splitkv, with the size
+ *                from fa_splitkv_workspace(B, H, Nq, max_blocks * block_size,
+ *                d, causal, ...)
+ *
+ * Errors: those of fa_fwd_paged and of fa_fwd_splitkv.
+ */
+fa_status fa_fwd_paged_splitkv(const void *Q, const void *K_cache, const void *V_cache, const int *block_table,
+                               const int *seq_lens, void *O, float *LSE, int B, int H, int Nq, int max_blocks,
+                               int num_blocks, int block_size, int d, float scale, int causal, int num_splits,
+                               void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
  * fa_bwd -- gradients of the attention forward ("6. FlashAttention 分块逻辑"
  * section 7; "9.4 FlashAttention 与 FlashMLA" sections 9.4.3 and 9.4.5): P is
  * recomputed tile by tile from Q, K and the forward's LSE, never stored, and

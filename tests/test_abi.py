@@ -109,3 +109,45 @@ def test_no_gpu_means_cuda_error_not_a_fallback(lib):
         pytest.skip("a GPU is present")
     # Valid arguments on a machine without a GPU: the call must fail loudly.
     assert call() == ops.FA_ERR_CUDA
+
+
+PAGED = dict(q=0x10000, kc=0x20000, vc=0x30000, table=0x60000, seq=0x70000, o=0x40000, lse=0x50000,
+             B=1, H=1, Nq=4, max_blocks=2, num_blocks=2, bs=64, d=64, scale=0.125, causal=0)
+
+
+@pytest.mark.parametrize("kw,expected", [
+    (dict(table=0), ops.FA_ERR_INVALID_ARG),
+    (dict(seq=0), ops.FA_ERR_INVALID_ARG),
+    (dict(max_blocks=0), ops.FA_ERR_INVALID_ARG),
+    (dict(num_blocks=0), ops.FA_ERR_INVALID_ARG),
+    (dict(bs=48), ops.FA_ERR_UNSUPPORTED),
+    (dict(bs=8), ops.FA_ERR_UNSUPPORTED),
+    (dict(bs=512), ops.FA_ERR_UNSUPPORTED),
+    (dict(table=0x60002), ops.FA_ERR_MISALIGNED),
+    (dict(seq=0x70001), ops.FA_ERR_MISALIGNED),
+    (dict(d=96), ops.FA_ERR_UNSUPPORTED),
+])
+@pytest.mark.parametrize("split", [False, True])
+def test_paged_argument_errors(lib, kw, expected, split):
+    a = dict(PAGED, **kw)
+    args = (a["q"], a["kc"], a["vc"], a["table"], a["seq"], a["o"], a["lse"], a["B"], a["H"], a["Nq"],
+            a["max_blocks"], a["num_blocks"], a["bs"], a["d"], a["scale"], a["causal"])
+    if split:
+        st = lib.fa_fwd_paged_splitkv(*args, 2, 0x100000, 1 << 30, None)
+    else:
+        st = lib.fa_fwd_paged(*args, None)
+    assert st == expected
+
+
+@pytest.mark.parametrize("splits,ws,nbytes,expected", [
+    (0, 0x100000, 1 << 30, ops.FA_ERR_INVALID_ARG),
+    (2, 0, 1 << 30, ops.FA_ERR_INVALID_ARG),
+    (2, 0x100010, 1 << 30, ops.FA_ERR_MISALIGNED),
+    (2, 0x100000, 64, ops.FA_ERR_INVALID_ARG),
+])
+def test_paged_splitkv_workspace_errors(lib, splits, ws, nbytes, expected):
+    a = PAGED
+    st = lib.fa_fwd_paged_splitkv(a["q"], a["kc"], a["vc"], a["table"], a["seq"], a["o"], a["lse"], a["B"], a["H"],
+                                  a["Nq"], a["max_blocks"], a["num_blocks"], a["bs"], a["d"], a["scale"],
+                                  a["causal"], splits, ws, nbytes, None)
+    assert st == expected

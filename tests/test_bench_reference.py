@@ -25,3 +25,26 @@ def test_reference_arm_other_ranks_exit_quietly():
                           "--steps", "1", "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=120,
                          env=env)
     assert out.returncode == 0 and out.stdout.strip() == ""
+
+
+def test_paged_cache_layout_reproduces_the_keys():
+    """bench --path paged scatters K/V into pages; reading them back through
+    the block table must give the contiguous tensors (CPU, no kernel)."""
+    torch = __import__("pytest").importorskip("torch")
+    sys.path.insert(0, ROOT)
+    import bench
+    B, H, Nk, d, bs = 3, 2, 150, 8, 16
+    g = torch.Generator().manual_seed(5)
+    k = torch.randn(B, H, Nk, d, generator=g)
+    v = torch.randn(B, H, Nk, d, generator=g)
+    kc, vc, table = bench.paged_cache(k, v, bs, seed=11)
+    nb = -(-Nk // bs)
+    assert kc.shape == (B * nb, H, bs, d) and table.shape == (B, nb) and table.dtype == torch.int32
+    assert sorted(table.flatten().tolist()) == list(range(B * nb))   # a permutation of the pages
+    for b in range(B):
+        for pos in range(Nk):
+            phy = int(table[b, pos // bs])
+            assert torch.equal(kc[phy, :, pos % bs], k[b, :, pos])
+            assert torch.equal(vc[phy, :, pos % bs], v[b, :, pos])
+    tail = Nk % bs
+    assert torch.count_nonzero(kc[int(table[0, nb - 1]), :, tail:]) == 0

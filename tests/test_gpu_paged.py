@@ -54,11 +54,11 @@ def make_case(seed, seq_lens, H, Nq, d, block_size, holes=0):
     return q, kc, vc, table, np.array(seq_lens, dtype=np.int32)
 
 
-def run_and_check(ops, q, kc, vc, table, seq_lens, causal, tag):
+def run_and_check(ops, q, kc, vc, table, seq_lens, causal, tag, num_splits=None):
     d = q.shape[-1]
     scale = float(np.float32(1 / math.sqrt(d)))
     o, lse = ops.fa_fwd_paged(to_dev(q), to_dev(kc), to_dev(vc), torch.from_numpy(table).cuda(),
-                              torch.from_numpy(seq_lens).cuda(), scale=scale, causal=causal)
+                              torch.from_numpy(seq_lens).cuda(), scale=scale, causal=causal, num_splits=num_splits)
     ops.check_device_status()
     O_ref, L_ref = paged.paged_attention(q, kc, vc, table, seq_lens, scale, causal)
     o = o.float().cpu().numpy().astype(np.float64)
@@ -98,5 +98,34 @@ def test_paged_full_prefill_equals_dense_forward(ops):
     seq = torch.tensor([N], dtype=torch.int32, device="cuda")
     o1, l1 = ops.fa_fwd_paged(to_dev(q), to_dev(kc), to_dev(vc), table, seq, causal=True)
     o2, l2 = ops.fa_fwd(to_dev(q), to_dev(k), to_dev(v), causal=True)
+    ops.check_device_status()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("num_splits", [2, 3, 8])
+@pytest.mark.parametrize("causal", [False, True])
+def test_paged_split_keys(ops, num_splits, causal):
+    # an empty sequence, a one-key one and long ones; slices of a short
+    # sequence are empty and must carry no weight in the merge
+    seq_lens = [0, 1, 300, 1000]
+    for Nq in (1, 5):
+        for bs in (16, 64):
+            q, kc, vc, table, sl = make_case(500 + bs + Nq, seq_lens, 2, Nq, 128, bs, holes=2)
+            run_and_check(ops, q, kc, vc, table, sl, causal, f"splits={num_splits} bs={bs} Nq={Nq} causal={causal}",
+                          num_splits=num_splits)
+
+
+def test_paged_split_decode_shape(ops):
+    # one query per head against 32768 keys in 64-key pages, slices chosen by the library
+    q, kc, vc, table, sl = make_case(901, [32768], 32, 1, 128, 64)
+    run_and_check(ops, q, kc, vc, table, sl, False, "decode auto splits", num_splits=0)
+    run_and_check(ops, q, kc, vc, table, sl, True, "decode auto splits causal", num_splits=0)
+
+
+def test_paged_split_one_slice_is_the_paged_forward(ops):
+    q, kc, vc, table, sl = make_case(33, [200, 450], 2, 64, 64, 32)
+    args = (to_dev(q), to_dev(kc), to_dev(vc), torch.from_numpy(table).cuda(), torch.from_numpy(sl).cuda())
+    o1, l1 = ops.fa_fwd_paged(*args, causal=True)
+    o2, l2 = ops.fa_fwd_paged(*args, causal=True, num_splits=1)
     ops.check_device_status()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
