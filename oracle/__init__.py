@@ -12,6 +12,8 @@ Contents
   partial-result merge, in numpy (``online.py``).
 * ``backward`` -- gradients of attention in fp64 (``backward.py``).
 * ``paged`` -- attention over a paged key/value cache (``paged.py``).
+* ``fp8`` -- E4M3 quantisation (with the Hadamard rotation of incoherent
+  processing) and attention on the dequantised inputs (``fp8.py``).
 
 Pinned by ``tests/test_oracle_pins.py``; every function has at least one pin
 that does not re-derive it from itself.
@@ -54,6 +56,13 @@ def load(path: str | None = None):
     f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                   ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                   ctypes.c_float, ctypes.c_int,
+                  ctypes.c_void_p, ctypes.c_int64,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    g = lib.oracle_attention_rows_f64
+    g.restype = ctypes.c_int
+    g.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                  ctypes.c_double, ctypes.c_int,
                   ctypes.c_void_p, ctypes.c_int64,
                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
     if path is None:
@@ -106,10 +115,33 @@ def attention(Q, K, V, scale, causal, nthreads=None, lib=None):
     return O.reshape(B, H, Nq, d), LSE.reshape(B, H, Nq)
 
 
+def attention_rows_f64(Q, K, V, scale, causal, rows=None, nthreads=None, lib=None):
+    """attention_rows on fp64 inputs (same layouts); `scale` is used as given."""
+    Q, K, V = (np.ascontiguousarray(a, dtype=np.float64) for a in (Q, K, V))
+    B, H, Nq, d = Q.shape
+    Nk = K.shape[2]
+    if K.shape != (B, H, Nk, d) or V.shape != (B, H, Nk, d):
+        raise ValueError("shape mismatch")
+    if rows is None:
+        nrows, rows_arr = B * H * Nq, None
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        nrows = rows_arr.size
+    O = np.empty((nrows, d), dtype=np.float64)
+    LSE = np.empty(nrows, dtype=np.float64)
+    rc = (lib or load()).oracle_attention_rows_f64(
+        Q.ctypes.data, K.ctypes.data, V.ctypes.data, B, H, Nq, Nk, d, float(scale), int(bool(causal)),
+        None if rows_arr is None else rows_arr.ctypes.data, nrows, O.ctypes.data, LSE.ctypes.data,
+        int(nthreads or os.cpu_count() or 1))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attention_rows_f64 failed with {rc}")
+    return O, LSE
+
+
 def bf16_bits_to_f64(a) -> np.ndarray:
     """Exact widening of bf16 bit patterns to fp64 (for numpy-side oracle pieces)."""
     a = _u16(a)
     return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-from . import paged  # noqa: E402,F401  (uses bf16_bits_to_f64 above)
+from . import fp8, paged  # noqa: E402,F401  (use bf16_bits_to_f64 / attention_rows_f64 above)

@@ -33,6 +33,9 @@
  *
  * Rows are independent, so the row list is split over `nthreads` POSIX
  * threads; each row is computed by the same sequential loops.
+ *
+ * oracle_attention_rows_f64 is the same computation on inputs given directly
+ * as fp64 arrays (used for inputs that are not bf16, e.g. dequantised FP8).
  */
 #include <math.h>
 #include <pthread.h>
@@ -77,8 +80,38 @@ static void attend_one_row(const uint16_t *q, const uint16_t *K, const uint16_t 
     *lse = m + log(l);
 }
 
+/* The same three passes on fp64 inputs. */
+static void attend_one_row_f64(const double *q, const double *K, const double *V,
+                               int64_t nvis, int64_t d, double scale,
+                               double *s, double *o, double *lse)
+{
+    for (int64_t j = 0; j < nvis; ++j) {
+        double acc = 0.0;
+        for (int64_t c = 0; c < d; ++c)
+            acc += q[c] * K[j * d + c];
+        s[j] = scale * acc;
+    }
+
+    double m = -INFINITY;
+    for (int64_t j = 0; j < nvis; ++j)
+        if (s[j] > m) m = s[j];
+
+    double l = 0.0;
+    for (int64_t j = 0; j < nvis; ++j)
+        l += exp(s[j] - m);
+
+    for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
+    for (int64_t j = 0; j < nvis; ++j) {
+        double p = exp(s[j] - m) / l;
+        for (int64_t c = 0; c < d; ++c)
+            o[c] += p * V[j * d + c];
+    }
+    *lse = m + log(l);
+}
+
 typedef struct {
     const uint16_t *Q, *K, *V;
+    const double *Qd, *Kd, *Vd;   /* fp64 inputs instead of bf16 when non-NULL */
     int64_t H, Nq, Nk, d;
     double scale;
     int causal;
@@ -99,11 +132,18 @@ static void *worker(void *arg)
         /* visible keys J_i: j < Nk, and j <= i when causal */
         int64_t nvis = jb->Nk;
         if (jb->causal && i + 1 < nvis) nvis = i + 1;
-        attend_one_row(jb->Q + r * jb->d,
-                       jb->K + bh * jb->Nk * jb->d,
-                       jb->V + bh * jb->Nk * jb->d,
-                       nvis, jb->d, jb->scale, s,
-                       jb->O + n * jb->d, jb->LSE + n);
+        if (jb->Qd)
+            attend_one_row_f64(jb->Qd + r * jb->d,
+                               jb->Kd + bh * jb->Nk * jb->d,
+                               jb->Vd + bh * jb->Nk * jb->d,
+                               nvis, jb->d, jb->scale, s,
+                               jb->O + n * jb->d, jb->LSE + n);
+        else
+            attend_one_row(jb->Q + r * jb->d,
+                           jb->K + bh * jb->Nk * jb->d,
+                           jb->V + bh * jb->Nk * jb->d,
+                           nvis, jb->d, jb->scale, s,
+                           jb->O + n * jb->d, jb->LSE + n);
     }
     free(s);
     return NULL;
@@ -113,13 +153,13 @@ static void *worker(void *arg)
  * Attention for the listed rows (all rows when `rows` is NULL, nrows = B*H*Nq).
  * Returns 0 on success, -1 on bad arguments, -2 on allocation/thread failure.
  */
-int oracle_attention_rows(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                          int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
-                          float scale, int causal,
-                          const int64_t *rows, int64_t nrows,
-                          double *O, double *LSE, int nthreads)
+static int run_rows(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                    const double *Qd, const double *Kd, const double *Vd,
+                    int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
+                    double scale, int causal,
+                    const int64_t *rows, int64_t nrows,
+                    double *O, double *LSE, int nthreads)
 {
-    if (!Q || !K || !V || !O || !LSE) return -1;
     if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1 || nrows < 0) return -1;
     if (rows) {
         for (int64_t n = 0; n < nrows; ++n)
@@ -138,8 +178,9 @@ int oracle_attention_rows(const uint16_t *Q, const uint16_t *K, const uint16_t *
     for (int t = 0; t < nthreads; ++t) {
         job_t *jb = &jobs[t];
         jb->Q = Q; jb->K = K; jb->V = V;
+        jb->Qd = Qd; jb->Kd = Kd; jb->Vd = Vd;
         jb->H = H; jb->Nq = Nq; jb->Nk = Nk; jb->d = d;
-        jb->scale = (double)scale;
+        jb->scale = scale;
         jb->causal = causal != 0;
         jb->rows = rows;
         jb->first = nrows * t / nthreads;
@@ -156,4 +197,26 @@ int oracle_attention_rows(const uint16_t *Q, const uint16_t *K, const uint16_t *
     free(jobs);
     free(tids);
     return rc;
+}
+
+int oracle_attention_rows(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                          int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
+                          float scale, int causal,
+                          const int64_t *rows, int64_t nrows,
+                          double *O, double *LSE, int nthreads)
+{
+    if (!Q || !K || !V || !O || !LSE) return -1;
+    return run_rows(Q, K, V, NULL, NULL, NULL, B, H, Nq, Nk, d, (double)scale, causal, rows, nrows, O, LSE,
+                    nthreads);
+}
+
+/* Inputs as fp64 arrays with the same layouts; `scale` is taken as given. */
+int oracle_attention_rows_f64(const double *Q, const double *K, const double *V,
+                              int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
+                              double scale, int causal,
+                              const int64_t *rows, int64_t nrows,
+                              double *O, double *LSE, int nthreads)
+{
+    if (!Q || !K || !V || !O || !LSE) return -1;
+    return run_rows(NULL, NULL, NULL, Q, K, V, B, H, Nq, Nk, d, scale, causal, rows, nrows, O, LSE, nthreads);
 }
