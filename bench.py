@@ -5,8 +5,8 @@
 
 One step = one fa_fwd launch over one batch of the workload (default: the
 non-causal B=2, H=16, N=4096, d=128 forward).  Prints one JSON line.
---path splitkv | bwd | paged times fa_fwd_splitkv, fa_bwd or fa_fwd_paged
-on the same workload instead.
+--path splitkv | bwd | paged | fp8 times fa_fwd_splitkv, fa_bwd,
+fa_fwd_paged or fa_fwd_fp8 on the same workload instead.
 
 * value: device-timed TFLOPS (4*B*H*Nq*Nk*d per step, halved when causal),
   inputs resident in HBM, K back-to-back steps bracketed by barrier + sync,
@@ -320,6 +320,28 @@ def run_ours(args, w):
     if args.path == "splitkv":
         splits, nbytes = ops.splitkv_workspace(w.B, w.H, w.Nq, w.Nk, w.d, w.causal, 0)
         workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    if args.path == "fp8":
+        # E4M3 codes of the inputs (Q, K rotated by the same random signs, V
+        # transposed), quantised once before timing; enough code sets that
+        # every step's inputs exceed L2
+        if w.d != 128:
+            raise SystemExit("--path fp8 needs d = 128")
+        signs = torch.from_numpy(np.random.default_rng(17).choice([-1.0, 1.0], size=w.d).astype(np.float32)).cuda()
+        fp8_bytes = w.B * w.H * (w.Nq * w.d + 2 * (-(-w.Nk // 16) * 16) * w.d + 2 * w.Nq * w.d + 4 * w.Nq)
+        n_fp8 = max(1, math.ceil(2 * L2_BYTES / fp8_bytes)) if fp8_bytes < 2 * L2_BYTES else 1
+        fp8_sets = []
+        for si in range(n_fp8):
+            s = sets[si % n_sets]
+            q8, dq = ops.quantize_fp8(s[0], signs)
+            k8, dk = ops.quantize_fp8(s[1], signs)
+            vt8, dv = ops.quantize_fp8(s[2], transpose=True)
+            fp8_sets.append((q8, k8, vt8, dq, dk, dv, torch.empty_like(s[3]), torch.empty_like(s[4])))
+        sets = sets[:1]
+        n_sets = 1
+        torch.cuda.synchronize()
+        ops.check_device_status()
+        l2_note = (f"rotating {n_fp8} E4M3 input sets, {n_fp8 * fp8_bytes / 2**20:.0f} MiB > 2x L2"
+                   if n_fp8 > 1 else f"E4M3 inputs {fp8_bytes / 2**20:.0f} MiB > 2x L2")
     if args.path == "paged":
         # each input set's K/V as a paged cache (same keys, scattered pages)
         seq_lens = torch.full((w.B,), w.Nk, dtype=torch.int32, device="cuda")
@@ -338,6 +360,10 @@ def run_ours(args, w):
             b = bwd_bufs[i % n_sets]
             ops.fa_bwd(s[0], s[1], s[2], s[3], s[4], b[0], b[1], b[2], b[3], scale=scale, causal=w.causal,
                        workspace=workspace, stream=stream)
+        elif args.path == "fp8":
+            f = fp8_sets[i % len(fp8_sets)]
+            ops.fa_fwd_fp8(f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7], scale=scale, causal=w.causal,
+                           stream=stream)
         elif args.path == "paged":
             kc, vc, table = paged_bufs[i % n_sets]
             ops.fa_fwd_paged(s[0], kc, vc, table, seq_lens, s[3], s[4], scale=scale, causal=w.causal, stream=stream,
@@ -389,27 +415,35 @@ def run_ours(args, w):
         # backward: five GEMMs of 2*Nq*Nk*d (dV, dP, dQ, dK and the recomputed S), 2.5x the forward
         flops = w.flops * 5 // 2 if args.path == "bwd" else w.flops
         value = aggregate_tflops(flops, ms_per_step, world)
-        ridge = float(peaks["bf16_tflops"]) * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
-        tensor_bound = flops / w.algorithmic_bytes >= ridge
+        # E4M3 contractions: the measured bf16 peak times the nominal fp8/bf16 ratio (4.5 / 2.25)
+        fp8 = args.path == "fp8"
+        tensor_peak = float(peaks["bf16_tflops"]) * (2.0 if fp8 else 1.0)
+        alg_bytes = (w.B * w.H * (w.Nq * w.d + 2 * w.Nk * w.d + 2 * w.Nq * w.d + 4 * w.Nq) if fp8
+                     else w.algorithmic_bytes)
+        ridge = tensor_peak * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
+        tensor_bound = flops / alg_bytes >= ridge
         if tensor_bound:
-            achieved, peak, unit, bound = flops / (launch_ms * 1e-3) / 1e12, float(peaks["bf16_tflops"]), \
-                "TFLOP/s", "tensor"
+            achieved, peak, unit, bound = flops / (launch_ms * 1e-3) / 1e12, tensor_peak, "TFLOP/s", "tensor"
         else:
-            achieved, peak, unit, bound = w.algorithmic_bytes / (launch_ms * 1e-3) / 1e9, float(peaks["hbm_gbs"]), \
+            achieved, peak, unit, bound = alg_bytes / (launch_ms * 1e-3) / 1e9, float(peaks["hbm_gbs"]), \
                 "GB/s", "hbm"
         traffic = profiled_traffic() if (w.name == DEFAULT_WORKLOAD and args.path == "fwd") else None
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0, sigma^2) rounded to bf16)",
+            "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16", "data": "synthetic (seeded N(0, sigma^2) rounded to bf16)",
             "config": dict(workload_config(w, l2_note, args), kv_splits=splits,
                            **({"block_size": args.block_size} if args.path == "paged" else {})),
             "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                          "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": f"{peak_src} " + ("bf16_tflops (burst)" if tensor_bound else "hbm_gbs"),
-                         "frac_of_sustained": (achieved / float(peaks.get("bf16_tflops_sustained", peak))
+                         "peak_source": f"{peak_src} " + (("bf16_tflops (burst) x 2, the nominal fp8/bf16 ratio"
+                                                            if fp8 else "bf16_tflops (burst)")
+                                                           if tensor_bound else "hbm_gbs"),
+                         "frac_of_sustained": (achieved / (float(peaks.get("bf16_tflops_sustained", peak))
+                                                           * (2.0 if fp8 else 1.0))
                                                if tensor_bound else None),
                          "kernel": ("fa_bwd_dot + fa_bwd_dkdv + fa_bwd_dq <%d>" % w.d if args.path == "bwd" else
+                                    "fa_fwd_kernel<128, 4> (E4M3)" if fp8 else
                                     "fa_fwd_kernel<%d, %d>" % (w.d, (2 if args.path == "paged" else 0) + (1 if splits > 1 else 0))
                                     + (" + fa_merge_kernel" if splits > 1 else "")),
                          "launch_ms": launch_ms},
@@ -443,9 +477,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     ap.add_argument("--block-size", type=int, default=64, help="page size of --path paged")
-    ap.add_argument("--path", choices=["fwd", "splitkv", "bwd", "paged"], default="fwd",
-                    help="fa_fwd, fa_fwd_splitkv with the library's slice count, fa_bwd, or "
-                         "fa_fwd_paged over the workload's K/V scattered into pages")
+    ap.add_argument("--path", choices=["fwd", "splitkv", "bwd", "paged", "fp8"], default="fwd",
+                    help="fa_fwd, fa_fwd_splitkv with the library's slice count, fa_bwd, "
+                         "fa_fwd_paged over the workload's K/V scattered into pages, or fa_fwd_fp8 on "
+                         "E4M3 codes of the workload (quantised before timing)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

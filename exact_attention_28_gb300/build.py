@@ -9,7 +9,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB_PATH = os.path.join(HERE, "libfa_gb300.so")
 SOURCES = ["fa_api.cu"]
-DEPENDS = ["fa_api.cu", "fa_fwd_kernel.cuh", "fa_bwd_kernel.cuh", "ptx_sm103.cuh", os.path.join("..", "..", "include", "fa.h")]
+DEPENDS = ["fa_api.cu", "fa_fwd_kernel.cuh", "fa_bwd_kernel.cuh", "fa_fp8_quant.cuh", "ptx_sm103.cuh", os.path.join("..", "..", "include", "fa.h")]
 
 
 def nvcc_command(out: str = LIB_PATH, extra=()):

@@ -10,6 +10,7 @@
 
 #include "../../include/fa.h"
 #include "fa_bwd_kernel.cuh"
+#include "fa_fp8_quant.cuh"
 #include "fa_fwd_kernel.cuh"
 
 namespace {
@@ -63,6 +64,23 @@ bool make_map_paged(CUtensorMap *map, const void *ptr, int num_blocks, int H, in
     const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(block_size < fa::kBC ? block_size : fa::kBC), 1, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 8-bit [BH][rows][inner] (inner bytes per row, a multiple of 16), boxes of
+// 128 bytes x box_rows rows x 1 head, 128-byte swizzle: E4M3 Q and K
+// ([BH][N][128], box 128 x 128) and V^T ([BH][128][ldn], box 128 keys x 128
+// channels).
+bool make_map_u8(CUtensorMap *map, const void *ptr, int64_t BH, int64_t rows, int64_t inner, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows) * inner};
+    const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(box_rows), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -178,6 +196,7 @@ size_t splitkv_bytes(int64_t BH, int Nq, int d, int splits) {
 struct DeviceInfo {
     int sms = 0;
     bool attr[2][4] = {};   // forward kernel [d == 128][mode] has its shared-memory limit set
+    bool attr_fp8 = false;  // the E4M3 forward (d = 128)
     bool bwd_attr64 = false, bwd_attr128 = false;
 };
 std::mutex g_dev_mu;
@@ -185,7 +204,7 @@ DeviceInfo g_dev[64];
 
 template <int D, int MODE>
 fa_status launch(const fa::FwdParams &p, int grid, cudaStream_t stream, bool &attr_done) {
-    using C = fa::Config<D>;
+    using C = fa::Config<D, (MODE & fa::kFp8) != 0>;
     if (!attr_done) {
         if (cudaFuncSetAttribute(fa::fa_fwd_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kSmemBytes) != cudaSuccess)
@@ -388,6 +407,67 @@ extern "C" fa_status fa_fwd_paged_splitkv(const void *Q, const void *K_cache, co
                    d, scale, causal, num_splits, O_part, LSE_part, s);
     if (st != FA_OK) return st;
     return run_merge(O_part, LSE_part, O, LSE, BH * Nq, d, num_splits, s);
+}
+
+// ------------------------------------------------------------------- E4M3
+
+extern "C" fa_status fa_fwd_fp8(const void *Q8, const void *K8, const void *Vt8, const float *descale_q,
+                                const float *descale_k, const float *descale_v, void *O, float *LSE, int B, int H,
+                                int Nq, int Nk, int d, float scale, int causal, fa_stream_t stream) {
+    fa_status st = validate(Q8, K8, Vt8, O, LSE, B, H, Nq, Nk, d, scale);
+    if (st != FA_OK) return st;
+    if (d != 128) return FA_ERR_UNSUPPORTED;
+    if (!descale_q || !descale_k || !descale_v) return FA_ERR_INVALID_ARG;
+    if (!aligned(descale_q, 4) || !aligned(descale_k, 4) || !aligned(descale_v, 4)) return FA_ERR_MISALIGNED;
+    int sms;
+    DeviceInfo *info;
+    st = device_info(sms, info);
+    if (st != FA_OK) return st;
+    fa::FwdParams p;
+    const int grid = setup_params(p, B, H, Nq, Nk, d, scale, causal, sms, 1);
+    const int64_t BH = static_cast<int64_t>(B) * H;
+    const int64_t ldn = (static_cast<int64_t>(Nk) + 15) / 16 * 16;
+    if (!make_map_u8(&p.tmQ, Q8, BH, Nq, d, fa::kBR) || !make_map_u8(&p.tmK, K8, BH, Nk, d, fa::kBC) ||
+        !make_map_u8(&p.tmV, Vt8, BH, d, ldn, d))
+        return FA_ERR_CUDA;
+    p.O = static_cast<__nv_bfloat16 *>(O);
+    p.LSE = LSE;
+    p.descale_q = descale_q;
+    p.descale_k = descale_k;
+    p.descale_v = descale_v;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    return launch<128, fa::kFp8>(p, grid, reinterpret_cast<cudaStream_t>(stream), info->attr_fp8);
+}
+
+extern "C" fa_status fa_quantize_fp8(const void *X, void *X8, float *descale, int B, int H, int N, int d,
+                                     const float *signs, int transpose, fa_stream_t stream) {
+    if (!X || !X8 || !descale) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    const int64_t BH = static_cast<int64_t>(B) * H;
+    const int64_t blocks = (static_cast<int64_t>(N) + fa::kQuantRows - 1) / fa::kQuantRows;
+    if (BH > (int64_t{1} << 30) || blocks > 65535) return FA_ERR_INVALID_ARG;
+    if (!aligned(X, 16) || !aligned(X8, 16) || !aligned(descale, 4) || (signs && !aligned(signs, 4)))
+        return FA_ERR_MISALIGNED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int ldn = (N + 15) / 16 * 16;
+    const dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(blocks));
+    const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(X);
+    uint8_t *x8 = static_cast<uint8_t *>(X8);
+    unsigned *amax = reinterpret_cast<unsigned *>(descale);
+    if (cudaMemsetAsync(descale, 0, static_cast<size_t>(BH) * 4, s) != cudaSuccess) return FA_ERR_CUDA;
+    if (d == 64) {
+        fa::fa_amax_kernel<64><<<grid, fa::kQuantThreads, 0, s>>>(x, signs, amax, N);
+        if (transpose) fa::fa_quant_kernel<64, true><<<grid, fa::kQuantThreads, 0, s>>>(x, signs, amax, x8, N, ldn);
+        else fa::fa_quant_kernel<64, false><<<grid, fa::kQuantThreads, 0, s>>>(x, signs, amax, x8, N, ldn);
+    } else {
+        fa::fa_amax_kernel<128><<<grid, fa::kQuantThreads, 0, s>>>(x, signs, amax, N);
+        if (transpose) fa::fa_quant_kernel<128, true><<<grid, fa::kQuantThreads, 0, s>>>(x, signs, amax, x8, N, ldn);
+        else fa::fa_quant_kernel<128, false><<<grid, fa::kQuantThreads, 0, s>>>(x, signs, amax, x8, N, ldn);
+    }
+    const float rs = signs ? static_cast<float>(1.0 / std::sqrt(static_cast<double>(d))) : 1.0f;
+    fa::fa_descale_kernel<<<static_cast<unsigned>((BH + 255) / 256), 256, 0, s>>>(descale, static_cast<int>(BH), rs);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 extern "C" fa_status fa_schedule(int B, int H, int Nq, int Nk, int d, int causal, int num_sms, int num_splits,

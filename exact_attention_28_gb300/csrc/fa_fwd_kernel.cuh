@@ -65,14 +65,21 @@ constexpr uint32_t kOtherRegs = 88;     // producer / MMA warpgroup
 static_assert(kSoftmaxRegs * 256 + kOtherRegs * 128 <= 168 * kThreads, "register split exceeds the launch allocation");
 constexpr int kChunkBytes = 128 * 128;  // one [128 rows x 64 bf16] swizzled TMA box
 constexpr float kTau = 8.0f;            // log2-domain slack before the max is raised
+// E4M3 P: a smaller slack and a headroom, p = 2^(c*s - m + 4) in (0, 2^8]:
+// the row maximum's weight lands in [2^4, 2^8] (E4M3 reaches 448), so keys
+// up to 14 log2 units below it stay above E4M3's smallest subnormal 2^-9
+// instead of 10 (with p <= 1 they would underflow and their mass be lost).
+constexpr float kTauF8 = 4.0f;
+constexpr float kHeadroomF8 = 4.0f;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait, then abort
 
 // Kernel variants, fixed at compile time so that the dense forward carries
-// none of the others' per-tile work.  Two independent bits:
+// none of the others' per-tile work.  Independent bits:
 //   kSplit -- items cut into key-range slices, fp32 partials (merged afterwards);
-//   kPaged -- K/V gathered from a block table, per-sequence key counts.
-// kDense (neither) reads contiguous K/V and writes bf16 O directly.
-enum Mode : int { kDense = 0, kSplit = 1, kPaged = 2, kPagedSplit = 3 };
+//   kPaged -- K/V gathered from a block table, per-sequence key counts;
+//   kFp8   -- E4M3 Q, K and transposed V with per-head scales, P in E4M3.
+// kDense (none) reads contiguous bf16 K/V and writes bf16 O directly.
+enum Mode : int { kDense = 0, kSplit = 1, kPaged = 2, kPagedSplit = 3, kFp8 = 4 };
 
 // Device status word: bit 0 = a pipeline wait expired, bit 1 = a shutdown
 // wait expired.  Read and cleared by the host.
@@ -80,20 +87,28 @@ __device__ unsigned int g_fa_status;
 // First failure: {block, role, item, step}.
 __device__ int g_fa_diag[4];
 
-template <int D>
+// Tile geometry.  bf16: a [128 rows][D] tile is D/64 boxes of [128][64].
+// E4M3 (D = 128 only): a Q or K tile is one box of [128 rows][128 bytes] and
+// a V tile is V^T's [D channel rows][128 keys], also one box.
+template <int D, bool F8 = false>
 struct Config {
     static_assert(D == 64 || D == 128, "head dimension");
-    static constexpr int kChunks = D / 64;                 // 128-byte swizzle chunks per row
-    static constexpr int kQTileBytes = kBR * D * 2;
-    static constexpr int kKVTileBytes = kBC * D * 2;
-    static constexpr int kSlots = (D == 128) ? 5 : 8;      // K/V ring depth (tiles)
+    static_assert(!F8 || D == 128, "the E4M3 path has D = 128 (one 128-byte row per tile row)");
+    static constexpr int kElem = F8 ? 1 : 2;
+    static constexpr int kChunks = D * kElem / 128;        // 128-byte swizzle chunks per row
+    static constexpr int kQTileBytes = kBR * D * kElem;
+    static constexpr int kKVTileBytes = kBC * D * kElem;
+    static constexpr int kSlots = F8 ? 10 : (D == 128 ? 5 : 8);   // K/V ring depth (tiles)
     static constexpr int kQBytes = 2 * kQTileBytes;
     static constexpr int kRingBytes = kSlots * kKVTileBytes;
     static constexpr int kBarOffset = kQBytes + kRingBytes;
     static constexpr int kSmemBytes = kBarOffset + 256 + 1024;  // + barriers, + alignment slack
     static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
-    static constexpr uint32_t kIdescS = ptx::instr_desc_bf16_f32(kBR, kBC, false, false);
-    static constexpr uint32_t kIdescPV = ptx::instr_desc_bf16_f32(kBR, D, false, true);
+    static constexpr uint32_t kIdescS =
+        F8 ? ptx::instr_desc_e4m3_f32(kBR, kBC) : ptx::instr_desc_bf16_f32(kBR, kBC, false, false);
+    // bf16: V [keys][D] is an MN-major B operand; E4M3: V^T [D][keys] is K-major
+    static constexpr uint32_t kIdescPV =
+        F8 ? ptx::instr_desc_e4m3_f32(kBR, D) : ptx::instr_desc_bf16_f32(kBR, D, false, true);
     static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -119,6 +134,9 @@ struct FwdParams {
     int H, block_size, max_blocks;
     const int *block_table;   // [B][max_blocks]; < 0: unallocated (its keys are skipped)
     const int *seq_lens;      // [B] keys per sequence
+    // E4M3 inputs (kFp8 kernels): the value of a code is code * descale[bh];
+    // tmV maps V^T [BH][D][ceil16(Nk)]
+    const float *descale_q, *descale_k, *descale_v;
     int causal;
     float c2;          // scale * log2(e)
 };
@@ -328,7 +346,7 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
 template <int D, int MODE>
 __device__ void producer_role(const FwdParams &p, const Shared &sh, uint32_t smem_q,
                               uint32_t smem_ring, uint32_t &loads_issued, uint32_t &q_arms) {
-    using C = Config<D>;
+    using C = Config<D, (MODE & kFp8) != 0>;
     const uint64_t pol_q = ptx::l2_policy_evict_first();
     const uint64_t pol_kv = ptx::l2_policy_evict_last();
     uint32_t it = 0;
@@ -372,6 +390,10 @@ __device__ void producer_role(const FwdParams &p, const Shared &sh, uint32_t sme
                 if constexpr ((MODE & kPaged) != 0) {
                     tma_load_paged_tile(p, map, smem_ring + slot * C::kKVTileBytes, full, item.bh % p.H, j, rows, pg,
                                         C::kChunks, pol_kv);
+                } else if constexpr ((MODE & kFp8) != 0) {
+                    // K: rows j*128.. of [Nk][128 B]; V^T: columns j*128.. of [D][ldn]
+                    ptx::tma_load_3d(smem_ring + slot * C::kKVTileBytes, map, full, which ? j * kBC : 0,
+                                     which ? 0 : j * kBC, item.bh, pol_kv);
                 } else {
                     #pragma unroll
                     for (int c = 0; c < C::kChunks; ++c)
@@ -390,16 +412,21 @@ __device__ void producer_role(const FwdParams &p, const Shared &sh, uint32_t sme
 // S_t = Q_t K_j^T: D/16 MMAs of K = 16.  Q and K tiles are D/64 boxes of
 // [128 rows][64 cols], 128-byte swizzled; step kk reads columns 16kk..16kk+15,
 // i.e. box kk/4 at byte offset 32*(kk%4) inside each 128-byte row.
-template <int D>
+// E4M3: D/32 MMAs of K = 32, the same 32-byte steps inside the one chunk.
+template <int D, bool F8 = false>
 __device__ __forceinline__ void issue_s(uint32_t tmem_s, uint32_t q_tile, uint32_t k_tile) {
-    using C = Config<D>;
+    using C = Config<D, F8>;
     constexpr uint32_t hi = ptx::sdesc_sw128_hi(1024);
     const uint32_t a0 = ptx::sdesc_sw128_lo(q_tile, 16);
     const uint32_t b0 = ptx::sdesc_sw128_lo(k_tile, 16);
+    constexpr int kSteps = D * C::kElem / 32;
     #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
+    for (int kk = 0; kk < kSteps; ++kk) {
         const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-        ptx::mma_bf16_ss(tmem_s, a0 + off, hi, b0 + off, hi, C::kIdescS, kk > 0 ? 1u : 0u);
+        if constexpr (F8)
+            ptx::mma_f8_ss(tmem_s, a0 + off, hi, b0 + off, hi, C::kIdescS, kk > 0 ? 1u : 0u);
+        else
+            ptx::mma_bf16_ss(tmem_s, a0 + off, hi, b0 + off, hi, C::kIdescS, kk > 0 ? 1u : 0u);
     }
 }
 
@@ -407,22 +434,35 @@ __device__ __forceinline__ void issue_s(uint32_t tmem_s, uint32_t q_tile, uint32
 // 8 columns of bf16 pairs per step).  V tile: [128 keys][D] as D/64 boxes of
 // [128][64]; the B operand is MN-major (D contiguous): 8-key groups SBO =
 // 1024 B apart, 64-column groups LBO = one box (16 KB) apart.
-template <int D>
+//
+// E4M3: 4 MMAs of K = 32 keys; P is 4 keys per TMEM column (8 columns per
+// step) and V^T [D rows][128 keys] is a K-major operand like K in S: 8-row
+// groups 1024 B apart, 32-byte steps along the keys.
+template <int D, bool F8 = false>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_tile,
                                          bool accumulate) {
-    using C = Config<D>;
+    using C = Config<D, F8>;
     constexpr uint32_t hi = ptx::sdesc_sw128_hi(1024);
-    const uint32_t b0 = ptx::sdesc_sw128_lo(v_tile, kChunkBytes);
-    #pragma unroll
-    for (int kk = 0; kk < kBC / 16; ++kk)
-        ptx::mma_bf16_ts(tmem_o, tmem_p + kk * 8, b0 + ((kk * 16 * 128) >> 4), hi, C::kIdescPV,
-                         (accumulate || kk > 0) ? 1u : 0u);
+    if constexpr (F8) {
+        const uint32_t b0 = ptx::sdesc_sw128_lo(v_tile, 16);
+        #pragma unroll
+        for (int kk = 0; kk < kBC / 32; ++kk)
+            ptx::mma_f8_ts(tmem_o, tmem_p + kk * 8, b0 + ((kk * 32) >> 4), hi, C::kIdescPV,
+                           (accumulate || kk > 0) ? 1u : 0u);
+    } else {
+        const uint32_t b0 = ptx::sdesc_sw128_lo(v_tile, kChunkBytes);
+        #pragma unroll
+        for (int kk = 0; kk < kBC / 16; ++kk)
+            ptx::mma_bf16_ts(tmem_o, tmem_p + kk * 8, b0 + ((kk * 16 * 128) >> 4), hi, C::kIdescPV,
+                             (accumulate || kk > 0) ? 1u : 0u);
+    }
 }
 
 template <int D, int MODE>
 __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, uint32_t smem_q,
                          uint32_t smem_ring) {
-    using C = Config<D>;
+    constexpr bool F8 = (MODE & kFp8) != 0;
+    using C = Config<D, F8>;
     uint32_t it = 0;
     uint32_t p_phase[2] = {0u, 0u};
     const uint32_t tS[2] = {tmem + 0u, tmem + 128u};
@@ -448,7 +488,7 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
         ptx::tc_fence_after_sync();
         for (int t = 0; t < 2; ++t) {
             if (item.nk[t] > kv0) {
-                issue_s<D>(tS[t], sQ[t], smem_ring + ks * C::kKVTileBytes);
+                issue_s<D, F8>(tS[t], sQ[t], smem_ring + ks * C::kKVTileBytes);
                 ptx::mma_commit(sh.s_full0 + 8 * t);
             }
         }
@@ -469,7 +509,7 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
                 if (!wait_bar(sh.p_full0, p_phase[0], sh.abort_flag, 1, w, j)) return;
                 p_phase[0] ^= 1u;
                 ptx::tc_fence_after_sync();
-                issue_pv<D>(tO[0], tS[0], v_tile, j > kv0);
+                issue_pv<D, F8>(tO[0], tS[0], v_tile, j > kv0);
                 if (j == nk0 - 1) ptx::mma_commit(sh.o_full0);
             }
             if (more) {
@@ -477,7 +517,7 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
                     return;
                 ptx::tc_fence_after_sync();
                 if (j + 1 < nk0) {
-                    issue_s<D>(tS[0], sQ[0], smem_ring + ks2 * C::kKVTileBytes);
+                    issue_s<D, F8>(tS[0], sQ[0], smem_ring + ks2 * C::kKVTileBytes);
                     ptx::mma_commit(sh.s_full0);
                 }
             }
@@ -485,13 +525,13 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
                 if (!wait_bar(sh.p_full0 + 8, p_phase[1], sh.abort_flag, 1, w, j)) return;
                 p_phase[1] ^= 1u;
                 ptx::tc_fence_after_sync();
-                issue_pv<D>(tO[1], tS[1], v_tile, j > kv0);
+                issue_pv<D, F8>(tO[1], tS[1], v_tile, j > kv0);
                 if (j == nk1 - 1) ptx::mma_commit(sh.o_full0 + 8);
             }
             ptx::mma_commit(sh.kv_empty0 + 8 * vs);
             if (more) {
                 if (j + 1 < nk1) {
-                    issue_s<D>(tS[1], sQ[1], smem_ring + ks2 * C::kKVTileBytes);
+                    issue_s<D, F8>(tS[1], sQ[1], smem_ring + ks2 * C::kKVTileBytes);
                     ptx::mma_commit(sh.s_full0 + 8);
                 }
                 ptx::mma_commit(sh.kv_empty0 + 8 * ks2);
@@ -571,14 +611,51 @@ __device__ __forceinline__ void exp_pack_store128(const uint32_t (&s)[128], floa
     sum_rounded = ((r[0] + r[1]) + (r[2] + r[3])) + ((r[4] + r[5]) + (r[6] + r[7]));
 }
 
+// E4M3 P: the same exponentials, packed four keys to a TMEM column (32
+// columns over the start of the S tile); the rounded sum adds the E4M3 values
+// (widened exactly) that P V uses.
+__device__ __forceinline__ void exp_pack_store128_e4m3(const uint32_t (&s)[128], float c2, float neg_m, uint32_t tP,
+                                                       float &sum_exact, float &sum_rounded) {
+    const uint64_t c2x2 = ptx::f2_pack(c2, c2), mx2 = ptx::f2_pack(neg_m, neg_m);
+    uint64_t acc_e[4];
+    #pragma unroll
+    for (int i = 0; i < 4; ++i) acc_e[i] = ptx::f2_pack(0.f, 0.f);
+    float r[8];
+    #pragma unroll
+    for (int i = 0; i < 8; ++i) r[i] = 0.f;
+    uint32_t pk[32];
+    #pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        float p[4];
+        #pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint64_t t = ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[4 * i + 2 * h]),
+                                                        __uint_as_float(s[4 * i + 2 * h + 1])), c2x2, mx2);
+            float t0, t1;
+            ptx::f2_unpack(t, t0, t1);
+            p[2 * h] = ptx::ex2(t0);
+            p[2 * h + 1] = ptx::ex2(t1);
+            acc_e[(2 * i + h) & 3] = ptx::f2_add(acc_e[(2 * i + h) & 3], ptx::f2_pack(p[2 * h], p[2 * h + 1]));
+        }
+        pk[i] = ptx::pack_e4m3x4(p[0], p[1], p[2], p[3]);
+        ptx::add_e4m3x4_to_f32(r[4 * (i & 1)], r[4 * (i & 1) + 1], r[4 * (i & 1) + 2], r[4 * (i & 1) + 3], pk[i]);
+    }
+    ptx::tmem_store_32cols(tP, pk);
+    float e0, e1;
+    ptx::f2_unpack(ptx::f2_add(ptx::f2_add(acc_e[0], acc_e[1]), ptx::f2_add(acc_e[2], acc_e[3])), e0, e1);
+    sum_exact = e0 + e1;
+    sum_rounded = ((r[0] + r[1]) + (r[2] + r[3])) + ((r[4] + r[5]) + (r[6] + r[7]));
+}
+
 template <int D, int MODE>
 __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem, int tile, int quad, int lane) {
     const int row = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tS = tmem + lane_off + tile * 128;
     const uint32_t tO = tmem + lane_off + 256 + tile * D;
-    const float c2 = p.c2;
-    const bool pos = c2 > 0.f;
+    constexpr bool F8 = (MODE & kFp8) != 0;
+    float c2 = p.c2;
+    const bool pos = c2 > 0.f;   // the descales are positive: the sign is the scale's
     // A masked key must never win the row extreme and must give p = 0:
     // -inf for a positive scale, +inf for a negative one (the host never
     // passes c2 == 0, see fa_fwd).
@@ -611,6 +688,16 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
             continue;
         }
         const int key_lim = p.causal ? min(item.seq_len, qg + 1 + item.q_shift) : item.seq_len;
+        [[maybe_unused]] float out_scale = 1.f;   // E4M3: V's descale
+        if constexpr (F8) {
+            // scores of the codes times descale_q * descale_k; kept a normal
+            // number (at least the smallest), like the host does for a zero
+            // scale: the flush-to-zero arithmetic below would read a subnormal
+            // as 0, and a masked key's -inf times 0 is NaN
+            c2 = p.c2 * __ldg(p.descale_q + item.bh) * __ldg(p.descale_k + item.bh);
+            if (fabsf(c2) < 1.17549435e-38f) c2 = pos ? 1.17549435e-38f : -1.17549435e-38f;
+            out_scale = __ldg(p.descale_v + item.bh);
+        }
         float m_ref = -INFINITY;   // log2-domain reference maximum
         float l = 0.f;             // sum of p (fp32), for LSE
         float l_rounded = 0.f;     // sum of the bf16 p that P V uses, for O
@@ -652,7 +739,7 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
             const float mx = row_extreme128(s, pos);
             const float m_tile = kvalid > 0 ? mx * c2 : -INFINITY;
             float alpha = 1.f;
-            if (m_tile > m_ref + kTau) {
+            if (m_tile > m_ref + (F8 ? kTauF8 : kTau)) {
                 alpha = ptx::ex2(m_ref - m_tile);   // 0 on the first visible tile
                 m_ref = m_tile;
             }
@@ -662,7 +749,10 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
             // m_ref is finite once a row has seen a key (every row sees key 0
             // in its first tile); the guard keeps a fully masked row at p = 0.
             float se, sr;
-            exp_pack_store128(s, c2, m_ref == -INFINITY ? 0.f : -m_ref, tS, se, sr);
+            if constexpr (F8)
+                exp_pack_store128_e4m3(s, c2, m_ref == -INFINITY ? 0.f : kHeadroomF8 - m_ref, tS, se, sr);
+            else
+                exp_pack_store128(s, c2, m_ref == -INFINITY ? 0.f : -m_ref, tS, se, sr);
             l += se;
             l_rounded += sr;
             // Rescale O_t in TMEM when this warp's reference maximum moved
@@ -687,9 +777,12 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
         o_phase ^= 1u;
         ptx::tc_fence_after_sync();
         // a row that saw no key at all (possible only with the paged cache) is empty: O = 0, LSE = -inf
-        const float inv_l = l_rounded > 0.f ? 1.f / l_rounded : 0.f;
+        float inv_l = l_rounded > 0.f ? 1.f / l_rounded : 0.f;
+        if constexpr (F8) inv_l *= out_scale;
         const bool live = qg < p.Nq;
-        const float lse = l > 0.f ? (m_ref + ptx::lg2(l)) * 0.69314718055994531f : -INFINITY;
+        // (the E4M3 weights carry the headroom factor 2^4: l does too, O not)
+        const float lse = l > 0.f ? (m_ref - (F8 ? kHeadroomF8 : 0.f) + ptx::lg2(l)) * 0.69314718055994531f
+                                  : -INFINITY;
         if constexpr ((MODE & kSplit) != 0) {
             // partial of this key slice: O / l in fp32 and its LSE
             float *prow_o = p.O_part + prow * D;
@@ -734,7 +827,7 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
 
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
-    using C = Config<D>;
+    using C = Config<D, (MODE & kFp8) != 0>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte-swizzled operand tiles.
     const uint32_t raw = ptx::smem_addr(smem_raw);

@@ -161,6 +161,29 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// The same two forms for 8-bit operands (kind::f8f6f4: K = 32 per MMA).
+__device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                          uint32_t b_hi, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "mov.b64 da, {%1, %2};\n\t"
+        "mov.b64 db, {%3, %4};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                          uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], db, %4, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 operation this thread issued
 // before this point has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -192,6 +215,12 @@ __host__ __device__ constexpr uint32_t instr_desc_bf16_f32(int M, int N, bool a_
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor for kind::f8f6f4 with E4M3 A and B (format code 0
+// at bits 7-9 and 10-12), both K-major, fp32 accumulator.
+__host__ __device__ constexpr uint32_t instr_desc_e4m3_f32(int M, int N) {
+    return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // ------------------------------------------------------- SFU / conversions
 
 __device__ __forceinline__ float ex2(float x) {
@@ -212,6 +241,34 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+
+// Four fp32 values to four E4M3 bytes (round to nearest even, saturating at
+// +-448); v0 goes to the lowest byte.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float v0, float v1, float v2, float v3) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r) : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+    return r;
+}
+// a0 += byte 0, a1 += byte 1, a2 += byte 2, a3 += byte 3 of four E4M3 values
+// (widened exactly through fp16, added in fp32 with a mixed-precision add).
+__device__ __forceinline__ void add_e4m3x4_to_f32(float &a0, float &a1, float &a2, float &a3, uint32_t w) {
+    asm("{\n\t.reg .b16 lo, hi, h0, h1, h2, h3;\n\t.reg .b32 wlo, whi;\n\t"
+        "mov.b32 {lo, hi}, %4;\n\t"
+        "cvt.rn.f16x2.e4m3x2 wlo, lo;\n\t"
+        "cvt.rn.f16x2.e4m3x2 whi, hi;\n\t"
+        "mov.b32 {h0, h1}, wlo;\n\t"
+        "mov.b32 {h2, h3}, whi;\n\t"
+        "add.rn.f32.f16 %0, h0, %0;\n\t"
+        "add.rn.f32.f16 %1, h1, %1;\n\t"
+        "add.rn.f32.f16 %2, h2, %2;\n\t"
+        "add.rn.f32.f16 %3, h3, %3;\n\t}"
+        : "+f"(a0), "+f"(a1), "+f"(a2), "+f"(a3)
+        : "r"(w));
+}
 
 // Packed pairs of fp32 (sm_100-family f32x2 arithmetic): one instruction
 // operates on both halves of a 64-bit register pair.

@@ -51,6 +51,10 @@ def load_library(path: str | None = None):
     lib.fa_fwd_paged_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, vp,
                                          ctypes.c_size_t, vp]
     lib.fa_fwd_paged_splitkv.restype = i
+    lib.fa_quantize_fp8.argtypes = [vp, vp, vp, i, i, i, i, vp, i, vp]
+    lib.fa_quantize_fp8.restype = i
+    lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd_fp8.restype = i
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, ctypes.c_size_t, vp]
     lib.fa_bwd.restype = i
     lib.fa_bwd_workspace.argtypes = [i, i, i, i, i, vp]
@@ -154,6 +158,44 @@ def fa_fwd_paged(q, k_cache, v_cache, block_table, seq_lens, o=None, lse=None, s
                                                lse.data_ptr(), B, H, Nq, max_blocks, num_blocks, block_size, d,
                                                scale, int(bool(causal)), splits, workspace.data_ptr(),
                                                workspace.numel() * workspace.element_size(), _stream_handle(stream)))
+    return o, lse
+
+
+def quantize_fp8(x, signs=None, transpose=False, stream=None):
+    """E4M3 codes (torch.uint8) and per-head descale (fp32 [B, H]) of a bf16
+    [B, H, N, d] CUDA tensor; `signs` (fp32 [d] of +-1, CUDA) rotates rows by
+    diag(signs) H / sqrt(d); transpose gives [B, H, d, ceil16(N)]."""
+    if not (x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()):
+        raise TypeError("x must be a contiguous bf16 CUDA tensor")
+    B, H, N, d = x.shape
+    if transpose:
+        x8 = torch.empty((B, H, d, -(-N // 16) * 16), dtype=torch.uint8, device=x.device)
+    else:
+        x8 = torch.empty((B, H, N, d), dtype=torch.uint8, device=x.device)
+    descale = torch.empty((B, H), dtype=torch.float32, device=x.device)
+    _check(load_library().fa_quantize_fp8(x.data_ptr(), x8.data_ptr(), descale.data_ptr(), B, H, N, d,
+                                          None if signs is None else signs.data_ptr(), int(bool(transpose)),
+                                          _stream_handle(stream)))
+    return x8, descale
+
+
+def fa_fwd_fp8(q8, k8, vt8, descale_q, descale_k, descale_v, o=None, lse=None, scale=None, causal=False,
+               stream=None):
+    """Attention on E4M3 codes: q8 [B,H,Nq,d], k8 [B,H,Nk,d], vt8 [B,H,d,ceil16(Nk)]
+    (torch.uint8 CUDA tensors) with per-head descales; returns bf16 O and fp32 LSE."""
+    B, H, Nq, d = q8.shape
+    Nk = k8.shape[2]
+    if k8.shape != (B, H, Nk, d) or vt8.shape != (B, H, d, -(-Nk // 16) * 16):
+        raise ValueError("shape mismatch")
+    if o is None:
+        o = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q8.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _check(load_library().fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), descale_q.data_ptr(),
+                                     descale_k.data_ptr(), descale_v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                     B, H, Nq, Nk, d, scale, int(bool(causal)), _stream_handle(stream)))
     return o, lse
 
 

@@ -186,6 +186,56 @@ fa_status fa_fwd_paged_splitkv(const void *Q, const void *K_cache, const void *V
                                void *workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /*
+ * fa_quantize_fp8 -- per-(batch, head) E4M3 quantisation of a bf16 tensor for
+ * fa_fwd_fp8 ("9.4 FlashAttention 与 FlashMLA", section 9.4.4: FlashAttention-3
+ * computes attention in FP8 and, before quantising, multiplies Q and K by a
+ * random orthogonal matrix -- "incoherent processing" -- which leaves Q K^T
+ * unchanged and spreads outlier channels over all channels).
+ *
+ *   X        bf16 [B, H, N, d], device memory, 16-byte aligned
+ *   signs    NULL, or device fp32 [d] of +1/-1: rotate each row by
+ *            M = diag(signs) H / sqrt(d) (H the Sylvester-Hadamard matrix,
+ *            applied as a fast Walsh-Hadamard transform).  Pass the same
+ *            signs for Q and K, and NULL for V.
+ *   transpose 0: X8 is E4M3 [B, H, N, d];  1: X8 is E4M3 [B, H, d, ldn] with
+ *            ldn = N rounded up to a multiple of 16 and zero padding (the V
+ *            layout fa_fwd_fp8 takes)
+ *   X8       output, device memory, 16-byte aligned
+ *   descale  output, device fp32 [B, H]: code * descale approximates the
+ *            (rotated) value; amax / 448 per head (/ sqrt(d) when rotated), 1
+ *            for a head of zeros
+ * Codes: round to nearest even of (rotated x) * (448 / amax), saturating;
+ * every step is one fp32 operation in a fixed order, so the result is the
+ * same on any launch.  Four stream operations (a clear of descale, then
+ * three kernels).
+ * Errors: FA_ERR_INVALID_ARG for NULL pointers, B, H, N < 1 or N above
+ * 4,194,240; FA_ERR_UNSUPPORTED for d not 64 or 128; FA_ERR_MISALIGNED.
+ */
+fa_status fa_quantize_fp8(const void *X, void *X8, float *descale, int B, int H, int N, int d,
+                          const float *signs, int transpose, fa_stream_t stream);
+
+/*
+ * fa_fwd_fp8 -- the attention forward on E4M3 inputs (FlashAttention-3's FP8
+ * mode, "9.4 FlashAttention 与 FlashMLA" section 9.4.4): S = Q K^T on the
+ * codes in one tcgen05 MMA kind (fp32 accumulation), scaled by
+ * scale * descale_q * descale_k; P rounded to E4M3 for P V (P in V's type,
+ * as the bf16 path rounds P to bf16); O = (P V) * descale_v / l in bf16.
+ *
+ *   Q8       E4M3 [B, H, Nq, d]      (fa_quantize_fp8, transpose = 0)
+ *   K8       E4M3 [B, H, Nk, d]      (transpose = 0; same signs as Q8)
+ *   Vt8      E4M3 [B, H, d, ldn]     (transpose = 1), ldn = Nk rounded up to
+ *            16; the padding columns must hold finite codes (0 does)
+ *   descale_q, descale_k, descale_v  device fp32 [B, H], positive
+ *   O, LSE, B, H, Nq, Nk, scale, causal, stream: as fa_fwd
+ *   d        128 only
+ * Errors: as fa_fwd (FA_ERR_UNSUPPORTED for d != 128); FA_ERR_INVALID_ARG
+ * for a NULL descale; FA_ERR_MISALIGNED for a descale not 4-byte aligned.
+ */
+fa_status fa_fwd_fp8(const void *Q8, const void *K8, const void *Vt8, const float *descale_q,
+                     const float *descale_k, const float *descale_v, void *O, float *LSE, int B, int H,
+                     int Nq, int Nk, int d, float scale, int causal, fa_stream_t stream);
+
+/*
  * fa_bwd -- gradients of the attention forward ("6. FlashAttention 分块逻辑"
  * section 7; "9.4 FlashAttention 与 FlashMLA" sections 9.4.3 and 9.4.5): P is
  * recomputed tile by tile from Q, K and the forward's LSE, never stored, and

@@ -151,3 +151,38 @@ def test_paged_splitkv_workspace_errors(lib, splits, ws, nbytes, expected):
                                   a["Nq"], a["max_blocks"], a["num_blocks"], a["bs"], a["d"], a["scale"],
                                   a["causal"], splits, ws, nbytes, None)
     assert st == expected
+
+
+@pytest.mark.parametrize("kw,expected", [
+    (dict(d=64), ops.FA_ERR_UNSUPPORTED),
+    (dict(dq=0), ops.FA_ERR_INVALID_ARG),
+    (dict(dv=0), ops.FA_ERR_INVALID_ARG),
+    (dict(dk=0x80002), ops.FA_ERR_MISALIGNED),
+    (dict(q=0x10008), ops.FA_ERR_MISALIGNED),
+    (dict(Nk=0), ops.FA_ERR_INVALID_ARG),
+])
+def test_fp8_forward_argument_errors(lib, kw, expected):
+    a = dict(q=0x10000, k=0x20000, v=0x30000, dq=0x80000, dk=0x80100, dv=0x80200, o=0x40000, lse=0x50000,
+             B=1, H=1, Nq=4, Nk=4, d=128, scale=0.125, causal=0)
+    a.update(kw)
+    st = lib.fa_fwd_fp8(a["q"], a["k"], a["v"], a["dq"], a["dk"], a["dv"], a["o"], a["lse"], a["B"], a["H"],
+                        a["Nq"], a["Nk"], a["d"], a["scale"], a["causal"], None)
+    assert st == expected
+
+
+@pytest.mark.parametrize("kw,expected", [
+    (dict(x=0), ops.FA_ERR_INVALID_ARG),
+    (dict(descale=0), ops.FA_ERR_INVALID_ARG),
+    (dict(N=0), ops.FA_ERR_INVALID_ARG),
+    (dict(N=65535 * 64 + 1), ops.FA_ERR_INVALID_ARG),
+    (dict(d=96), ops.FA_ERR_UNSUPPORTED),
+    (dict(x=0x10002), ops.FA_ERR_MISALIGNED),
+    (dict(x8=0x20004), ops.FA_ERR_MISALIGNED),
+    (dict(signs=0x30002), ops.FA_ERR_MISALIGNED),
+])
+def test_quantize_argument_errors(lib, kw, expected):
+    a = dict(x=0x10000, x8=0x20000, descale=0x40000, B=1, H=1, N=4, d=128, signs=0, transpose=0)
+    a.update(kw)
+    st = lib.fa_quantize_fp8(a["x"], a["x8"], a["descale"], a["B"], a["H"], a["N"], a["d"], a["signs"] or None,
+                             a["transpose"], None)
+    assert st == expected
