@@ -15,16 +15,18 @@
 //                       dV += P^T dO, dK += dS^T Q
 //   fa_bwd_dq_kernel    one CTA per 128-query tile, looping over key tiles
 //                       (Q-outer): S = Q K^T, dP = dO V^T, dS, dQ += dS K
-// Each CTA is one warpgroup: thread t owns TMEM lane t (a key in the first
-// kernel, a query in the second); thread 0 issues the TMA loads and MMAs.
-// Loads are double-buffered; every wait is bounded like the forward's.
+// Each CTA has 5 warps: thread t < 128 owns TMEM lane t (a key in the first
+// kernel, a query in the second) and does the elementwise work; thread 128
+// issues the TMA loads and MMAs, so that the elementwise phases of one step
+// overlap the GEMMs of the neighbouring ones.  Loads are double-buffered;
+// every wait is bounded like the forward's.
 #pragma once
 
 #include "fa_fwd_kernel.cuh"
 
 namespace fa {
 
-constexpr int kBwdThreads = 128;
+constexpr int kBwdThreads = 160;   // warps 0-3: elementwise (thread = TMEM lane), warp 4: loads + MMAs
 
 struct BwdParams {
     CUtensorMap tmQ, tmK, tmV, tmdO;   // [BH][N][D] bf16, box {64, 128, 1}, 128-byte swizzle
@@ -72,11 +74,15 @@ __global__ void __launch_bounds__(256) fa_bwd_dot_kernel(const __nv_bfloat16 *__
 
 // ------------------------------------------------------------------ shared
 
+// Barriers of both kernels (one arrival unless noted).
 struct BwdShared {
     uint32_t load0;     // + 8 * stage: TMA tiles of a stage landed
     uint32_t first;     // the resident pair of tiles landed
-    uint32_t mma_s;     // the two score-side GEMMs of an iteration completed
-    uint32_t mma_acc0;  // + 8 * stage: the accumulating GEMMs that read a stage completed
+    uint32_t sfull;     // the score GEMM of the current step completed
+    uint32_t dpfull;    // the dP GEMM of the current step completed
+    uint32_t pready;    // (128) phase A done: P stored (dK/dV) or S read into registers (dQ)
+    uint32_t dsready;   // (128) phase B done: dS stored
+    uint32_t acc0;      // + 8 * stage: the accumulating GEMMs that read a stage completed
     uint32_t done;
     volatile int *abort_flag;
 };
@@ -92,13 +98,12 @@ __device__ __forceinline__ void bwd_load_pair(const CUtensorMap *a, const CUtens
     }
 }
 
-// Thread-block barrier for the elementwise -> MMA hand-off: every thread's
-// TMEM stores are complete and visible to the MMA issued next.
-__device__ __forceinline__ void tmem_stores_to_mma() {
+// This thread's TMEM stores are complete and ordered before its arrival on
+// `bar`, which the MMA warp waits for before reading them.
+__device__ __forceinline__ void tmem_stores_then_arrive(uint32_t bar) {
     ptx::tmem_wait_store();
     ptx::tc_fence_before_sync();
-    __syncthreads();
-    ptx::tc_fence_after_sync();
+    ptx::mbar_arrive(bar);
 }
 
 // Writes one TMEM row of D fp32 columns, times `mul`, as bf16 to global.
@@ -120,51 +125,54 @@ __device__ __forceinline__ void store_row_bf16(uint32_t taddr, float mul, __nv_b
     }
 }
 
-// The elementwise step shared by both kernels, for one TMEM row of 128
-// score columns: P = 2^(c*s - lse2), dS = P * (dP - D), with masked columns
-// giving P = dS = 0.  Column q's lse2 and D come from `col_lse2`/`col_d`
-// (the first kernel: per query column) or are the row's own (the second).
-// P (if wanted) and dS are packed to bf16 pairs and written over the first 64
-// columns of the score region and of the dP region respectively.
-template <bool kWantP, bool kPerColumnStats>
-__device__ __forceinline__ void bwd_elementwise(uint32_t tS, uint32_t tdP, float c2, const float *col_lse2,
-                                                const float *col_d, float row_lse2, float row_d, int col_lo,
-                                                int col_hi) {
-    // columns c with col_lo <= c < col_hi are visible (others: P = 0)
-    #pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-        uint32_t s[64], dp[64];
-        ptx::tmem_load_32cols(tS + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-        ptx::tmem_load_32cols(tS + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-        ptx::tmem_load_32cols(tdP + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
-        ptx::tmem_load_32cols(tdP + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
-        uint32_t pk[32], dk[32];
+// Phase A of one TMEM row of 128 score columns: P = 2^(c*s - lse2) for the
+// visible columns col_lo <= c < col_hi, 0 elsewhere (column c's lse2 is
+// col_lse2[c] when kPerColumn -- the dK/dV kernel, one query per column --
+// else the row's own).  P stays in registers (fp32) for phase B; with
+// kStoreP it is also written as bf16 pairs over the score region's first 64
+// columns (the A operand of dV += P^T dO).
+template <bool kPerColumn, bool kStoreP>
+__device__ __forceinline__ void bwd_phase_a(const uint32_t (&sv)[128], float (&pv)[128], uint32_t tS, float c2,
+                                            const float *col_lse2, float row_lse2, int col_lo, int col_hi) {
+    #pragma unroll
+    for (int c = 0; c < 128; ++c) {
+        const float lse2 = kPerColumn ? col_lse2[c] : row_lse2;
+        const float e = ptx::ex2(fmaf(__uint_as_float(sv[c]), c2, -lse2));
+        pv[c] = (c >= col_lo && c < col_hi) ? e : 0.f;
+    }
+    if constexpr (kStoreP) {
         #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            float pv[2], dv[2];
+        for (int q = 0; q < 4; ++q) {
+            uint32_t pk[16];
             #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int c = 64 * half + 2 * i + e;
-                const float lse2 = kPerColumnStats ? col_lse2[c] : row_lse2;
-                const float dd = kPerColumnStats ? col_d[c] : row_d;
-                float p = ptx::ex2(fmaf(__uint_as_float(s[2 * i + e]), c2, -lse2));
-                p = (c >= col_lo && c < col_hi) ? p : 0.f;
-                pv[e] = p;
-                dv[e] = p * (__uint_as_float(dp[2 * i + e]) - dd);
-            }
-            pk[i] = ptx::pack_bf16x2(pv[0], pv[1]);
-            dk[i] = ptx::pack_bf16x2(dv[0], dv[1]);
+            for (int i = 0; i < 16; ++i) pk[i] = ptx::pack_bf16x2(pv[32 * q + 2 * i], pv[32 * q + 2 * i + 1]);
+            ptx::tmem_store_16cols(tS + 16 * q, pk);
         }
-        if (kWantP) {
-            ptx::tmem_store_16cols(tS + 32 * half, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
-            ptx::tmem_store_16cols(tS + 32 * half + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
-        }
-        ptx::tmem_store_16cols(tdP + 32 * half, *reinterpret_cast<const uint32_t(*)[16]>(&dk[0]));
-        ptx::tmem_store_16cols(tdP + 32 * half + 16, *reinterpret_cast<const uint32_t(*)[16]>(&dk[16]));
     }
 }
 
-// Shared set-up of both kernels: smem carve-up, barriers, TMEM allocation.
+// Phase B: dS = P * (dP - D) over the 128 columns, in quarters of 32 (each
+// quarter's dS goes to columns 16q.., already read), as bf16 pairs over the
+// dP region's first 64 columns (the A operand of the dK or dQ GEMM).
+template <bool kPerColumn>
+__device__ __forceinline__ void bwd_phase_b(const float (&pv)[128], uint32_t tdP, const float *col_d, float row_d) {
+    #pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t dp[32];
+        ptx::tmem_load_32cols(tdP + 32 * q, dp);
+        uint32_t dk[16];
+        #pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int c = 32 * q + 2 * i;
+            const float d0 = kPerColumn ? col_d[c] : row_d, d1 = kPerColumn ? col_d[c + 1] : row_d;
+            dk[i] = ptx::pack_bf16x2(pv[c] * (__uint_as_float(dp[2 * i]) - d0),
+                                     pv[c + 1] * (__uint_as_float(dp[2 * i + 1]) - d1));
+        }
+        ptx::tmem_store_16cols(tdP + 16 * q, dk);
+    }
+}
+
+// Set-up of both kernels: smem carve-up, barriers, TMEM allocation by warp 4.
 template <int D>
 __device__ __forceinline__ uint32_t bwd_setup(uint8_t *smem_raw, uint32_t &base, uint8_t *&base_ptr, BwdShared &sh) {
     using C = BwdConfig<D>;
@@ -174,23 +182,29 @@ __device__ __forceinline__ uint32_t bwd_setup(uint8_t *smem_raw, uint32_t &base,
     const uint32_t bars = base + C::kBarOffset;
     sh.load0 = bars + 0;      // 2
     sh.first = bars + 16;
-    sh.mma_s = bars + 24;
-    sh.mma_acc0 = bars + 32;  // 2
-    sh.done = bars + 48;
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(base_ptr + C::kBarOffset + 64);
-    sh.abort_flag = reinterpret_cast<volatile int *>(base_ptr + C::kBarOffset + 68);
+    sh.sfull = bars + 24;
+    sh.dpfull = bars + 32;
+    sh.pready = bars + 40;
+    sh.dsready = bars + 48;
+    sh.acc0 = bars + 56;      // 2
+    sh.done = bars + 72;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(base_ptr + C::kBarOffset + 80);
+    sh.abort_flag = reinterpret_cast<volatile int *>(base_ptr + C::kBarOffset + 84);
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(sh.load0 + 8 * i, 1);
-            ptx::mbar_init(sh.mma_acc0 + 8 * i, 1);
+            ptx::mbar_init(sh.acc0 + 8 * i, 1);
         }
         ptx::mbar_init(sh.first, 1);
-        ptx::mbar_init(sh.mma_s, 1);
+        ptx::mbar_init(sh.sfull, 1);
+        ptx::mbar_init(sh.dpfull, 1);
+        ptx::mbar_init(sh.pready, 128);
+        ptx::mbar_init(sh.dsready, 128);
         ptx::mbar_init(sh.done, 1);
         *sh.abort_flag = 0;
         ptx::fence_barrier_init();
     }
-    if (threadIdx.x < 32) {
+    if ((threadIdx.x >> 5) == 4) {
         ptx::tmem_alloc(ptx::smem_addr(tmem_holder), C::kTmemCols);
         ptx::tmem_relinquish_alloc_permit();
     }
@@ -200,25 +214,148 @@ __device__ __forceinline__ uint32_t bwd_setup(uint8_t *smem_raw, uint32_t &base,
     return *tmem_holder;
 }
 
+// Teardown: the MMA thread (128) waits for all its MMAs and drains the TMA
+// loads it issued (issued[s] loads on stage s), then warp 4 frees TMEM.
 template <int D>
-__device__ __forceinline__ void bwd_teardown(uint32_t tmem, const BwdShared &sh) {
+__device__ __forceinline__ void bwd_teardown(uint32_t tmem, const BwdShared &sh, const int (&issued)[2],
+                                             bool first_issued) {
+    if (threadIdx.x == 128) {
+        ptx::mma_commit(sh.done);
+        wait_drain(sh.done, 0);
+        for (int s = 0; s < 2; ++s)
+            if (issued[s] > 0) wait_drain(sh.load0 + 8 * s, (issued[s] - 1) & 1);
+        if (first_issued) wait_drain(sh.first, 0);
+    }
     ptx::tc_fence_before_sync();
     __syncthreads();
-    if (threadIdx.x < 32) {
-        if (threadIdx.x == 0) {
-            ptx::mma_commit(sh.done);
-            wait_drain(sh.done, 0);
-        }
-        __syncwarp();
+    if ((threadIdx.x >> 5) == 4) {
         ptx::tc_fence_after_sync();
         ptx::tmem_dealloc(tmem, BwdConfig<D>::kTmemCols);
     }
 }
 
 // ------------------------------------------------------------ dK, dV kernel
-
+//
 // TMEM: S^T [0,128) (P^T as bf16 pairs in [0,64)), dP^T [128,256) (dS^T in
 // [128,192)), dV [256, 256+D), dK [256+D, 256+2D).  Lane = key.
+// Warps 0-3: thread t = key j*128 + t, elementwise.  Warp 4, lane 0: loads
+// and MMAs, per query tile n:
+//   wait P^T(n) -> dV += P^T dO_n;  S^T(n+1) = K Q_{n+1}^T     (S^T free once P^T is read)
+//   wait dS^T(n) -> dK += dS^T Q_n; dP^T(n+1) = V dO_{n+1}^T
+// so phase A of step n+1 runs while dK(n) and dP^T(n+1) execute, and phase
+// B of step n while dV(n) and S^T(n+1) do.
+
+template <int D>
+__device__ void dkdv_mma_role(const BwdParams &p, const BwdShared &sh, uint32_t tmem, uint32_t base, int j, int bh,
+                              int i_begin, int n_i, int (&issued)[2], bool &first_issued) {
+    using C = BwdConfig<D>;
+    const uint32_t sK = base, sV = base + C::kTile;
+    const uint32_t sQ[2] = {base + 2 * C::kTile, base + 3 * C::kTile};
+    const uint32_t sdO[2] = {base + 4 * C::kTile, base + 5 * C::kTile};
+    const uint32_t tST = tmem + 0, tdPT = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
+    constexpr int kChunks = D / 64;
+    ptx::mbar_arrive_expect_tx(sh.first, 2 * C::kTile);
+    first_issued = true;
+    {
+        const uint64_t pol = ptx::l2_policy_evict_first();
+        for (int c = 0; c < kChunks; ++c) {
+            ptx::tma_load_3d(sK + c * kChunkBytes, &p.tmK, sh.first, c * 64, j * kBC, bh, pol);
+            ptx::tma_load_3d(sV + c * kChunkBytes, &p.tmV, sh.first, c * 64, j * kBC, bh, pol);
+        }
+    }
+    for (int s = 0; s < 2 && s < n_i; ++s) {
+        bwd_load_pair(&p.tmQ, &p.tmdO, sQ[s], sdO[s], sh.load0 + 8 * s, (i_begin + s) * kBR, bh, kChunks, C::kTile);
+        ++issued[s];
+    }
+    if (!wait_bar(sh.first, 0, sh.abort_flag, 10, blockIdx.x, -1)) return;
+    if (!wait_bar(sh.load0, 0, sh.abort_flag, 10, blockIdx.x, 0)) return;
+    ptx::tc_fence_after_sync();
+    issue_s<D>(tST, sK, sQ[0]);      // S^T(0) = K Q_0^T
+    ptx::mma_commit(sh.sfull);
+    issue_s<D>(tdPT, sV, sdO[0]);    // dP^T(0) = V dO_0^T
+    ptx::mma_commit(sh.dpfull);
+    for (int n = 0; n < n_i; ++n) {
+        const int s = n & 1;
+        if (!wait_bar(sh.pready, n & 1, sh.abort_flag, 11, blockIdx.x, n)) return;
+        ptx::tc_fence_after_sync();
+        issue_pv<D>(tdV, tST, sdO[s], n > 0);                 // dV += P^T dO_n
+        if (n + 1 < n_i) {
+            if (!wait_bar(sh.load0 + 8 * (s ^ 1), ((n + 1) >> 1) & 1, sh.abort_flag, 12, blockIdx.x, n + 1)) return;
+            ptx::tc_fence_after_sync();
+            issue_s<D>(tST, sK, sQ[s ^ 1]);                   // S^T(n+1)
+            ptx::mma_commit(sh.sfull);
+        }
+        if (!wait_bar(sh.dsready, n & 1, sh.abort_flag, 13, blockIdx.x, n)) return;
+        ptx::tc_fence_after_sync();
+        issue_pv<D>(tdK, tdPT, sQ[s], n > 0);                 // dK += dS^T Q_n
+        ptx::mma_commit(sh.acc0 + 8 * s);                     // stage s read for the last time
+        if (n + 1 < n_i) {
+            issue_s<D>(tdPT, sV, sdO[s ^ 1]);                 // dP^T(n+1)
+            ptx::mma_commit(sh.dpfull);
+        }
+        if (n + 2 < n_i) {   // refill stage s once its readers are done
+            if (!wait_bar(sh.acc0 + 8 * s, (n >> 1) & 1, sh.abort_flag, 14, blockIdx.x, n)) return;
+            bwd_load_pair(&p.tmQ, &p.tmdO, sQ[s], sdO[s], sh.load0 + 8 * s, (i_begin + n + 2) * kBR, bh, kChunks,
+                          C::kTile);
+            ++issued[s];
+        }
+    }
+}
+
+template <int D>
+__device__ void dkdv_elementwise_role(const BwdParams &p, const BwdShared &sh, uint32_t tmem, float *stat, int j,
+                                      int bh, int i_begin, int n_i) {
+    const int t = threadIdx.x;
+    const uint32_t lane_off = static_cast<uint32_t>((t >> 5) * 32) << 16;
+    const uint32_t tST = tmem + lane_off, tdPT = tmem + lane_off + 128;
+    const uint32_t tdV = tmem + lane_off + 256, tdK = tmem + lane_off + 256 + D;
+    const int key = j * kBC + t;
+    const size_t out_row = (static_cast<size_t>(bh) * p.Nk + key) * D;
+    if (n_i <= 0) {   // no query sees this key
+        if (key < p.Nk)
+            for (int c = 0; c < D; ++c) p.dV[out_row + c] = p.dK[out_row + c] = __float2bfloat16_rn(0.f);
+        return;
+    }
+    bool ok = true;
+    for (int n = 0; n < n_i; ++n) {
+        const int i = i_begin + n;
+        const int s = n & 1;
+        {   // per-query statistics of this tile, in log2 units; padding rows masked
+            const int q = i * kBR + t;
+            const bool live = q < p.Nq;
+            stat[(s * 2 + 0) * 128 + t] = live ? p.LSE[static_cast<size_t>(bh) * p.Nq + q] * 1.4426950408889634f
+                                               : INFINITY;
+            stat[(s * 2 + 1) * 128 + t] = live ? p.Dsum[static_cast<size_t>(bh) * p.Nq + q] : 0.f;
+        }
+        // publishes the statistics; every thread leaves the loop together
+        if (!ptx::named_barrier_and(1, 128, ok)) { ok = false; break; }
+        if (!wait_bar(sh.sfull, n & 1, sh.abort_flag, 15, blockIdx.x, n)) { ok = false; continue; }
+        ptx::tc_fence_after_sync();
+        // visible query columns for this key: all, or those at or after the key
+        // on the diagonal tile; a key past Nk has none
+        const int col_lo = key >= p.Nk ? kBR : (p.causal && i == j ? t : 0);
+        float pv[128];
+        {
+            uint32_t sv[128];
+            ptx::tmem_load_128cols(tST, sv);
+            bwd_phase_a<true, true>(sv, pv, tST, p.c2, stat + (s * 2 + 0) * 128, 0.f, col_lo, kBR);
+        }
+        tmem_stores_then_arrive(sh.pready);
+        if (!wait_bar(sh.dpfull, n & 1, sh.abort_flag, 16, blockIdx.x, n)) { ok = false; continue; }
+        ptx::tc_fence_after_sync();
+        bwd_phase_b<true>(pv, tdPT, stat + (s * 2 + 1) * 128, 0.f);
+        tmem_stores_then_arrive(sh.dsready);
+    }
+    if (!ptx::named_barrier_and(1, 128, ok)) return;
+    // the last accumulation done: dV and scale * dK for this key
+    const int s = (n_i - 1) & 1;
+    if (!wait_bar(sh.acc0 + 8 * s, ((n_i - 1) >> 1) & 1, sh.abort_flag, 17, blockIdx.x, n_i)) return;
+    ptx::tc_fence_after_sync();
+    const bool live = key < p.Nk;
+    store_row_bf16<D>(tdV, 1.f, p.dV + out_row, live);
+    store_row_bf16<D>(tdK, p.scale, p.dK + out_row, live);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
     using C = BwdConfig<D>;
@@ -227,123 +364,119 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
     uint8_t *base_ptr;
     BwdShared sh;
     const uint32_t tmem = bwd_setup<D>(smem_raw, base, base_ptr, sh);
-    const int t = threadIdx.x;
-    const int warp = t >> 5;
-
     // heavy tiles (small j under the causal mask) get the low block indices
     const int j = blockIdx.x / p.BH;
     const int bh = blockIdx.x % p.BH;
     const int i_begin = p.causal ? j : 0;      // query tiles that can see key tile j
     const int n_i = p.Tr - i_begin;
-    const uint32_t sK = base, sV = base + C::kTile;
-    const uint32_t sQ[2] = {base + 2 * C::kTile, base + 3 * C::kTile};
-    const uint32_t sdO[2] = {base + 4 * C::kTile, base + 5 * C::kTile};
-    float *stat = reinterpret_cast<float *>(base_ptr + C::kStatOffset);   // [2][2][128]: lse2, D
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tST = tmem + 0, tdPT = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
-    constexpr int kChunks = D / 64;
-    bool ok = true;
-
-    if (t == 0 && n_i > 0) {
-        ptx::mbar_arrive_expect_tx(sh.first, 2 * C::kTile);
-        const uint64_t pol = ptx::l2_policy_evict_first();
-        for (int c = 0; c < kChunks; ++c) {
-            ptx::tma_load_3d(sK + c * kChunkBytes, &p.tmK, sh.first, c * 64, j * kBC, bh, pol);
-            ptx::tma_load_3d(sV + c * kChunkBytes, &p.tmV, sh.first, c * 64, j * kBC, bh, pol);
-        }
-        for (int s = 0; s < 2 && s < n_i; ++s)
-            bwd_load_pair(&p.tmQ, &p.tmdO, sQ[s], sdO[s], sh.load0 + 8 * s, (i_begin + s) * kBR, bh, kChunks,
-                          C::kTile);
+    int issued[2] = {0, 0};
+    bool first_issued = false;
+    if (threadIdx.x < 128) {
+        dkdv_elementwise_role<D>(p, sh, tmem, reinterpret_cast<float *>(base_ptr + C::kStatOffset), j, bh, i_begin,
+                                 n_i);
+    } else if (threadIdx.x == 128 && n_i > 0) {
+        dkdv_mma_role<D>(p, sh, tmem, base, j, bh, i_begin, n_i, issued, first_issued);
     }
-    const int key = j * kBC + t;
-    // every failure decision below is made block-wide (__syncthreads_and), so
-    // all threads leave the loop together and meet at the same barriers
-    for (int n = 0; n < n_i; ++n) {
-        const int i = i_begin + n;
-        const int s = n & 1;
-        const uint32_t use = n >> 1;
-        // per-query statistics of this tile, in log2 units, padding rows masked
-        {
-            const int q = i * kBR + t;
-            const bool live = q < p.Nq;
-            stat[(s * 2 + 0) * 128 + t] = live ? p.LSE[static_cast<size_t>(bh) * p.Nq + q] * 1.4426950408889634f
-                                               : INFINITY;
-            stat[(s * 2 + 1) * 128 + t] = live ? p.Dsum[static_cast<size_t>(bh) * p.Nq + q] : 0.f;
-        }
-        bool step_ok = true;
-        if (t == 0) {
-            if (n == 0) step_ok = wait_bar(sh.first, 0, sh.abort_flag, 10, blockIdx.x, -1);
-            step_ok = step_ok && wait_bar(sh.load0 + 8 * s, use & 1, sh.abort_flag, 10, blockIdx.x, n);
-            if (step_ok) {
-                ptx::tc_fence_after_sync();
-                issue_s<D>(tmem + tST, sK, sQ[s]);      // S^T = K_j Q_i^T
-                issue_s<D>(tmem + tdPT, sV, sdO[s]);    // dP^T = V_j dO_i^T
-                ptx::mma_commit(sh.mma_s);
-            }
-        }
-        if (!__syncthreads_and(step_ok)) { ok = false; break; }   // also publishes the statistics
-        if (!__syncthreads_and(wait_bar(sh.mma_s, n & 1, sh.abort_flag, 11, blockIdx.x, n))) { ok = false; break; }
-        ptx::tc_fence_after_sync();
-        // visible query columns for this key: all, or those at or after the key
-        // on the diagonal tile; a key past Nk has none
-        const int col_lo = key >= p.Nk ? kBR : (p.causal && i == j ? t : 0);
-        bwd_elementwise<true, true>(tmem + lane_off + tST, tmem + lane_off + tdPT, p.c2, stat + (s * 2 + 0) * 128,
-                                    stat + (s * 2 + 1) * 128, 0.f, 0.f, col_lo, kBR);
-        tmem_stores_to_mma();
-        step_ok = true;
-        if (t == 0) {
-            issue_pv<D>(tmem + tdV, tmem + tST, sdO[s], n > 0);   // dV += P^T dO_i
-            issue_pv<D>(tmem + tdK, tmem + tdPT, sQ[s], n > 0);   // dK += dS^T Q_i
-            ptx::mma_commit(sh.mma_acc0 + 8 * s);
-            if (n + 2 < n_i) {   // refill this stage once its readers are done
-                step_ok = wait_bar(sh.mma_acc0 + 8 * s, use & 1, sh.abort_flag, 12, blockIdx.x, n);
-                if (step_ok)
-                    bwd_load_pair(&p.tmQ, &p.tmdO, sQ[s], sdO[s], sh.load0 + 8 * s, (i + 2) * kBR, bh, kChunks,
-                                  C::kTile);
-            }
-        }
-        // the stage's statistics may be rewritten two iterations later
-        if (!__syncthreads_and(step_ok)) { ok = false; break; }
-    }
-    // wait for the last accumulation, then write dV and scale * dK for this key
-    if (n_i > 0 && ok) {
-        const int s = (n_i - 1) & 1;
-        const uint32_t use = (n_i - 1) >> 1;
-        if (wait_bar(sh.mma_acc0 + 8 * s, use & 1, sh.abort_flag, 13, blockIdx.x, n_i)) {
-            ptx::tc_fence_after_sync();
-            const bool live = key < p.Nk;
-            const size_t row = (static_cast<size_t>(bh) * p.Nk + key) * D;
-            store_row_bf16<D>(tmem + lane_off + tdV, 1.f, p.dV + row, live);
-            store_row_bf16<D>(tmem + lane_off + tdK, p.scale, p.dK + row, live);
-        }
-    } else if (n_i <= 0 && key < p.Nk) {   // no query sees this key
-        const size_t row = (static_cast<size_t>(bh) * p.Nk + key) * D;
-        for (int c = 0; c < D; ++c) p.dV[row + c] = p.dK[row + c] = __float2bfloat16_rn(0.f);
-    }
-    // drain outstanding loads before the CTA's shared memory is released
-    if (t == 0)
-        for (int s = 0; s < 2 && s < n_i; ++s) {
-            const int last = (n_i - 1 - s) >= 0 ? ((n_i - 1 - s) / 2) * 2 + s : -1;
-            if (last >= 0) wait_drain(sh.load0 + 8 * s, (last >> 1) & 1);
-        }
-    bwd_teardown<D>(tmem, sh);
+    __syncwarp();
+    bwd_teardown<D>(tmem, sh, issued, first_issued);
 }
 
 // --------------------------------------------------------------- dQ kernel
-
+//
 // TMEM: S [0,128), dP [128,256) (dS as bf16 pairs in [128,192)), dQ [256, 256+D).
-// Lane = query.
+// Lane = query.  Warp 4, lane 0, per key tile n:
+//   wait S(n) read -> S(n+1) = Q K_{n+1}^T   (S(n) is in the threads' registers)
+//   wait dS(n)     -> dQ += dS K_n;  dP(n+1) = dO V_{n+1}^T
+
+template <int D>
+__device__ void dq_mma_role(const BwdParams &p, const BwdShared &sh, uint32_t tmem, uint32_t base, int i, int bh,
+                            int n_j, int (&issued)[2], bool &first_issued) {
+    using C = BwdConfig<D>;
+    const uint32_t sQ = base, sdO = base + C::kTile;
+    const uint32_t sK[2] = {base + 2 * C::kTile, base + 3 * C::kTile};
+    const uint32_t sV[2] = {base + 4 * C::kTile, base + 5 * C::kTile};
+    const uint32_t tS = tmem + 0, tdP = tmem + 128, tdQ = tmem + 256;
+    constexpr int kChunks = D / 64;
+    bwd_load_pair(&p.tmQ, &p.tmdO, sQ, sdO, sh.first, i * kBR, bh, kChunks, C::kTile);
+    first_issued = true;
+    for (int s = 0; s < 2 && s < n_j; ++s) {
+        bwd_load_pair(&p.tmK, &p.tmV, sK[s], sV[s], sh.load0 + 8 * s, s * kBC, bh, kChunks, C::kTile);
+        ++issued[s];
+    }
+    if (!wait_bar(sh.first, 0, sh.abort_flag, 20, blockIdx.x, -1)) return;
+    if (!wait_bar(sh.load0, 0, sh.abort_flag, 20, blockIdx.x, 0)) return;
+    ptx::tc_fence_after_sync();
+    issue_s<D>(tS, sQ, sK[0]);      // S(0) = Q K_0^T
+    ptx::mma_commit(sh.sfull);
+    issue_s<D>(tdP, sdO, sV[0]);    // dP(0) = dO V_0^T
+    ptx::mma_commit(sh.dpfull);
+    for (int n = 0; n < n_j; ++n) {
+        const int s = n & 1;
+        if (!wait_bar(sh.pready, n & 1, sh.abort_flag, 21, blockIdx.x, n)) return;
+        if (n + 1 < n_j) {
+            if (!wait_bar(sh.load0 + 8 * (s ^ 1), ((n + 1) >> 1) & 1, sh.abort_flag, 22, blockIdx.x, n + 1)) return;
+            ptx::tc_fence_after_sync();
+            issue_s<D>(tS, sQ, sK[s ^ 1]);                    // S(n+1)
+            ptx::mma_commit(sh.sfull);
+        }
+        if (!wait_bar(sh.dsready, n & 1, sh.abort_flag, 23, blockIdx.x, n)) return;
+        ptx::tc_fence_after_sync();
+        issue_pv<D>(tdQ, tdP, sK[s], n > 0);                  // dQ += dS K_n
+        if (n + 1 < n_j) {
+            issue_s<D>(tdP, sdO, sV[s ^ 1]);                  // dP(n+1)
+            ptx::mma_commit(sh.dpfull);
+        }
+        ptx::mma_commit(sh.acc0 + 8 * s);                     // stage s read for the last time
+        if (n + 2 < n_j) {
+            if (!wait_bar(sh.acc0 + 8 * s, (n >> 1) & 1, sh.abort_flag, 24, blockIdx.x, n)) return;
+            bwd_load_pair(&p.tmK, &p.tmV, sK[s], sV[s], sh.load0 + 8 * s, (n + 2) * kBC, bh, kChunks, C::kTile);
+            ++issued[s];
+        }
+    }
+}
+
+template <int D>
+__device__ void dq_elementwise_role(const BwdParams &p, const BwdShared &sh, uint32_t tmem, int i, int bh, int n_j) {
+    const int t = threadIdx.x;
+    const uint32_t lane_off = static_cast<uint32_t>((t >> 5) * 32) << 16;
+    const uint32_t tS = tmem + lane_off, tdP = tmem + lane_off + 128, tdQ = tmem + lane_off + 256;
+    const int q = i * kBR + t;
+    const bool qlive = q < p.Nq;
+    const float row_lse2 = qlive ? p.LSE[static_cast<size_t>(bh) * p.Nq + q] * 1.4426950408889634f : INFINITY;
+    const float row_d = qlive ? p.Dsum[static_cast<size_t>(bh) * p.Nq + q] : 0.f;
+    for (int n = 0; n < n_j; ++n) {
+        if (!wait_bar(sh.sfull, n & 1, sh.abort_flag, 25, blockIdx.x, n)) return;
+        ptx::tc_fence_after_sync();
+        // visible key columns: below Nk, and at or before the query on the diagonal
+        int col_hi = min(kBC, p.Nk - n * kBC);
+        if (p.causal && n == i) col_hi = min(col_hi, t + 1);
+        if (!qlive) col_hi = 0;
+        float pv[128];
+        {
+            uint32_t sv[128];
+            ptx::tmem_load_128cols(tS, sv);
+            ptx::tc_fence_before_sync();
+            ptx::mbar_arrive(sh.pready);   // S(n) is in registers: its columns may be overwritten
+            bwd_phase_a<false, false>(sv, pv, tS, p.c2, nullptr, row_lse2, 0, col_hi);
+        }
+        if (!wait_bar(sh.dpfull, n & 1, sh.abort_flag, 26, blockIdx.x, n)) return;
+        ptx::tc_fence_after_sync();
+        bwd_phase_b<false>(pv, tdP, nullptr, row_d);
+        tmem_stores_then_arrive(sh.dsready);
+    }
+    const int s = (n_j - 1) & 1;
+    if (!wait_bar(sh.acc0 + 8 * s, ((n_j - 1) >> 1) & 1, sh.abort_flag, 27, blockIdx.x, n_j)) return;
+    ptx::tc_fence_after_sync();
+    store_row_bf16<D>(tdQ, p.scale, p.dQ + (static_cast<size_t>(bh) * p.Nq + q) * D, qlive);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
-    using C = BwdConfig<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint32_t base;
     uint8_t *base_ptr;
     BwdShared sh;
     const uint32_t tmem = bwd_setup<D>(smem_raw, base, base_ptr, sh);
-    const int t = threadIdx.x;
-    const int warp = t >> 5;
-
     // heavy tiles (large i under the causal mask) get the low block indices
     const int i = p.causal ? (p.Tr - 1 - blockIdx.x / p.BH) : blockIdx.x / p.BH;
     const int bh = blockIdx.x % p.BH;
@@ -352,75 +485,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
         const int q_end = min(p.Nq, (i + 1) * kBR);
         n_j = min(p.Tc, (q_end - 1) / kBC + 1);
     }
-    const uint32_t sQ = base, sdO = base + C::kTile;
-    const uint32_t sK[2] = {base + 2 * C::kTile, base + 3 * C::kTile};
-    const uint32_t sV[2] = {base + 4 * C::kTile, base + 5 * C::kTile};
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tS = tmem + 0, tdP = tmem + 128, tdQ = tmem + 256;
-    constexpr int kChunks = D / 64;
-    const int q = i * kBR + t;
-    const bool qlive = q < p.Nq;
-    const float row_lse2 = qlive ? p.LSE[static_cast<size_t>(bh) * p.Nq + q] * 1.4426950408889634f : INFINITY;
-    const float row_d = qlive ? p.Dsum[static_cast<size_t>(bh) * p.Nq + q] : 0.f;
-    bool ok = true;
-
-    if (t == 0) {
-        bwd_load_pair(&p.tmQ, &p.tmdO, sQ, sdO, sh.first, i * kBR, bh, kChunks, C::kTile);
-        for (int s = 0; s < 2 && s < n_j; ++s)
-            bwd_load_pair(&p.tmK, &p.tmV, sK[s], sV[s], sh.load0 + 8 * s, s * kBC, bh, kChunks, C::kTile);
-    }
-    for (int n = 0; n < n_j; ++n) {
-        const int jj = n;
-        const int s = n & 1;
-        const uint32_t use = n >> 1;
-        bool step_ok = true;
-        if (t == 0) {
-            if (n == 0) step_ok = wait_bar(sh.first, 0, sh.abort_flag, 14, blockIdx.x, -1);
-            step_ok = step_ok && wait_bar(sh.load0 + 8 * s, use & 1, sh.abort_flag, 14, blockIdx.x, n);
-            if (step_ok) {
-                ptx::tc_fence_after_sync();
-                issue_s<D>(tmem + tS, sQ, sK[s]);     // S = Q_i K_j^T
-                issue_s<D>(tmem + tdP, sdO, sV[s]);   // dP = dO_i V_j^T
-                ptx::mma_commit(sh.mma_s);
-            }
-        }
-        if (!__syncthreads_and(step_ok)) { ok = false; break; }
-        if (!__syncthreads_and(wait_bar(sh.mma_s, n & 1, sh.abort_flag, 15, blockIdx.x, n))) { ok = false; break; }
-        ptx::tc_fence_after_sync();
-        // visible key columns: below Nk, and at or before the query on the diagonal
-        int col_hi = min(kBC, p.Nk - jj * kBC);
-        if (p.causal && jj == i) col_hi = min(col_hi, t + 1);
-        if (!qlive) col_hi = 0;
-        bwd_elementwise<false, false>(tmem + lane_off + tS, tmem + lane_off + tdP, p.c2, nullptr, nullptr,
-                                      row_lse2, row_d, 0, col_hi);
-        tmem_stores_to_mma();
-        step_ok = true;
-        if (t == 0) {
-            issue_pv<D>(tmem + tdQ, tmem + tdP, sK[s], n > 0);   // dQ += dS K_j
-            ptx::mma_commit(sh.mma_acc0 + 8 * s);
-            if (n + 2 < n_j) {
-                step_ok = wait_bar(sh.mma_acc0 + 8 * s, use & 1, sh.abort_flag, 16, blockIdx.x, n);
-                if (step_ok)
-                    bwd_load_pair(&p.tmK, &p.tmV, sK[s], sV[s], sh.load0 + 8 * s, (jj + 2) * kBC, bh, kChunks,
-                                  C::kTile);
-            }
-        }
-        if (!__syncthreads_and(step_ok)) { ok = false; break; }
-    }
-    if (ok) {
-        const int s = (n_j - 1) & 1;
-        const uint32_t use = (n_j - 1) >> 1;
-        if (wait_bar(sh.mma_acc0 + 8 * s, use & 1, sh.abort_flag, 17, blockIdx.x, n_j)) {
-            ptx::tc_fence_after_sync();
-            store_row_bf16<D>(tmem + lane_off + tdQ, p.scale, p.dQ + (static_cast<size_t>(bh) * p.Nq + q) * D, qlive);
-        }
-    }
-    if (t == 0)
-        for (int s = 0; s < 2 && s < n_j; ++s) {
-            const int last = ((n_j - 1 - s) / 2) * 2 + s;
-            wait_drain(sh.load0 + 8 * s, (last >> 1) & 1);
-        }
-    bwd_teardown<D>(tmem, sh);
+    int issued[2] = {0, 0};
+    bool first_issued = false;
+    if (threadIdx.x < 128) dq_elementwise_role<D>(p, sh, tmem, i, bh, n_j);
+    else if (threadIdx.x == 128) dq_mma_role<D>(p, sh, tmem, base, i, bh, n_j, issued, first_issued);
+    __syncwarp();
+    bwd_teardown<D>(tmem, sh, issued, first_issued);
 }
 
 }  // namespace fa

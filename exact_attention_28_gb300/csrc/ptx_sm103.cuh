@@ -300,6 +300,17 @@ __device__ __forceinline__ void add_bf16x2_to_f32(float &acc_lo, float &acc_hi, 
         : "+f"(acc_lo), "+f"(acc_hi)
         : "r"(w));
 }
+// Named barrier `id` over `count` threads that also ANDs a predicate over
+// them (bar.red.and): every participant gets the same result.
+__device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t count, bool pred) {
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\t"
+                 "setp.ne.b32 p, %1, 0;\n\t"
+                 "bar.red.and.pred q, %2, %3, p;\n\t"
+                 "selp.b32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r) : "r"(pred ? 1u : 0u), "r"(id), "r"(count) : "memory");
+    return r != 0;
+}
 // Three-input maximum / minimum.
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float r;
