@@ -134,11 +134,19 @@ __device__ __forceinline__ void store_row_bf16(uint32_t taddr, float mul, __nv_b
 template <bool kPerColumn, bool kStoreP>
 __device__ __forceinline__ void bwd_phase_a(const uint32_t (&sv)[128], float (&pv)[128], uint32_t tS, float c2,
                                             const float *col_lse2, float row_lse2, int col_lo, int col_hi) {
+    // the statistics as float4 reads of shared memory (one per 4 columns)
+    const bool full = __all_sync(0xffffffffu, col_lo <= 0 && col_hi >= 128);   // warp-uniform
     #pragma unroll
-    for (int c = 0; c < 128; ++c) {
-        const float lse2 = kPerColumn ? col_lse2[c] : row_lse2;
-        const float e = ptx::ex2(fmaf(__uint_as_float(sv[c]), c2, -lse2));
-        pv[c] = (c >= col_lo && c < col_hi) ? e : 0.f;
+    for (int c = 0; c < 128; c += 4) {
+        float4 l4 = make_float4(row_lse2, row_lse2, row_lse2, row_lse2);
+        if constexpr (kPerColumn) l4 = *reinterpret_cast<const float4 *>(col_lse2 + c);
+        const float l[4] = {l4.x, l4.y, l4.z, l4.w};
+        #pragma unroll
+        for (int e = 0; e < 4; ++e) pv[c + e] = ptx::ex2(fmaf(__uint_as_float(sv[c + e]), c2, -l[e]));
+    }
+    if (!full) {
+        #pragma unroll
+        for (int c = 0; c < 128; ++c) pv[c] = (c >= col_lo && c < col_hi) ? pv[c] : 0.f;
     }
     if constexpr (kStoreP) {
         #pragma unroll
@@ -162,11 +170,14 @@ __device__ __forceinline__ void bwd_phase_b(const float (&pv)[128], uint32_t tdP
         ptx::tmem_load_32cols(tdP + 32 * q, dp);
         uint32_t dk[16];
         #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 16; i += 2) {
             const int c = 32 * q + 2 * i;
-            const float d0 = kPerColumn ? col_d[c] : row_d, d1 = kPerColumn ? col_d[c + 1] : row_d;
-            dk[i] = ptx::pack_bf16x2(pv[c] * (__uint_as_float(dp[2 * i]) - d0),
-                                     pv[c + 1] * (__uint_as_float(dp[2 * i + 1]) - d1));
+            float4 d4 = make_float4(row_d, row_d, row_d, row_d);
+            if constexpr (kPerColumn) d4 = *reinterpret_cast<const float4 *>(col_d + c);
+            dk[i] = ptx::pack_bf16x2(pv[c] * (__uint_as_float(dp[2 * i]) - d4.x),
+                                     pv[c + 1] * (__uint_as_float(dp[2 * i + 1]) - d4.y));
+            dk[i + 1] = ptx::pack_bf16x2(pv[c + 2] * (__uint_as_float(dp[2 * i + 2]) - d4.z),
+                                         pv[c + 3] * (__uint_as_float(dp[2 * i + 3]) - d4.w));
         }
         ptx::tmem_store_16cols(tdP + 16 * q, dk);
     }
