@@ -15,18 +15,19 @@
 //                       dV += P^T dO, dK += dS^T Q
 //   fa_bwd_dq_kernel    one CTA per 128-query tile, looping over key tiles
 //                       (Q-outer): S = Q K^T, dP = dO V^T, dS, dQ += dS K
-// Each CTA has 5 warps: thread t < 128 owns TMEM lane t (a key in the first
+// Each CTA has 6 warps: thread t < 128 owns TMEM lane t (a key in the first
 // kernel, a query in the second) and does the elementwise work; thread 128
-// issues the TMA loads and MMAs, so that the elementwise phases of one step
-// overlap the GEMMs of the neighbouring ones.  Loads are double-buffered;
-// every wait is bounded like the forward's.
+// issues the MMAs, so that the elementwise phases of one step overlap the
+// GEMMs of the neighbouring ones; thread 160 issues the TMA loads, refilling
+// each tile of a double-buffered stage as soon as its last GEMM has read it.
+// Every wait is bounded like the forward's.
 #pragma once
 
 #include "fa_fwd_kernel.cuh"
 
 namespace fa {
 
-constexpr int kBwdThreads = 160;   // warps 0-3: elementwise (thread = TMEM lane), warp 4: loads + MMAs
+constexpr int kBwdThreads = 192;   // warps 0-3: elementwise (thread = TMEM lane), warp 4: MMAs, warp 5: loads
 
 struct BwdParams {
     CUtensorMap tmQ, tmK, tmV, tmdO;   // [BH][N][D] bf16, box {64, 128, 1}, 128-byte swizzle
@@ -75,17 +76,27 @@ __global__ void __launch_bounds__(256) fa_bwd_dot_kernel(const __nv_bfloat16 *__
 // ------------------------------------------------------------------ shared
 
 // Barriers of both kernels (one arrival unless noted).
+// A stage holds two streamed tiles, A and B: Q and dO in the dK/dV kernel,
+// K and V in the dQ kernel.
 struct BwdShared {
-    uint32_t load0;     // + 8 * stage: TMA tiles of a stage landed
+    uint32_t loadA0, loadB0;   // + 8 * stage: the tile landed
+    uint32_t freeA0, freeB0;   // + 8 * stage: the last GEMM reading the tile completed
     uint32_t first;     // the resident pair of tiles landed
     uint32_t sfull;     // the score GEMM of the current step completed
     uint32_t dpfull;    // the dP GEMM of the current step completed
     uint32_t pready;    // (128) phase A done: P stored (dK/dV) or S read into registers (dQ)
     uint32_t dsready;   // (128) phase B done: dS stored
-    uint32_t acc0;      // + 8 * stage: the accumulating GEMMs that read a stage completed
     uint32_t done;
     volatile int *abort_flag;
 };
+
+// One tile (D/64 boxes) into `dst`, completing on `bar`.
+__device__ __forceinline__ void bwd_load_tile(const CUtensorMap *map, uint32_t dst, uint32_t bar, int row, int bh,
+                                              int chunks, int tile_bytes) {
+    ptx::mbar_arrive_expect_tx(bar, tile_bytes);
+    const uint64_t pol = ptx::l2_policy_evict_last();
+    for (int c = 0; c < chunks; ++c) ptx::tma_load_3d(dst + c * kChunkBytes, map, bar, c * 64, row, bh, pol);
+}
 
 __device__ __forceinline__ void bwd_load_pair(const CUtensorMap *a, const CUtensorMap *b, uint32_t dst_a,
                                               uint32_t dst_b, uint32_t bar, int row, int bh, int chunks,
@@ -191,20 +202,24 @@ __device__ __forceinline__ uint32_t bwd_setup(uint8_t *smem_raw, uint32_t &base,
     base = (raw + 1023u) & ~1023u;
     base_ptr = smem_raw + (base - raw);
     const uint32_t bars = base + C::kBarOffset;
-    sh.load0 = bars + 0;      // 2
-    sh.first = bars + 16;
-    sh.sfull = bars + 24;
-    sh.dpfull = bars + 32;
-    sh.pready = bars + 40;
-    sh.dsready = bars + 48;
-    sh.acc0 = bars + 56;      // 2
-    sh.done = bars + 72;
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(base_ptr + C::kBarOffset + 80);
-    sh.abort_flag = reinterpret_cast<volatile int *>(base_ptr + C::kBarOffset + 84);
+    sh.loadA0 = bars + 0;     // 2
+    sh.loadB0 = bars + 16;    // 2
+    sh.freeA0 = bars + 32;    // 2
+    sh.freeB0 = bars + 48;    // 2
+    sh.first = bars + 64;
+    sh.sfull = bars + 72;
+    sh.dpfull = bars + 80;
+    sh.pready = bars + 88;
+    sh.dsready = bars + 96;
+    sh.done = bars + 104;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(base_ptr + C::kBarOffset + 112);
+    sh.abort_flag = reinterpret_cast<volatile int *>(base_ptr + C::kBarOffset + 116);
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
-            ptx::mbar_init(sh.load0 + 8 * i, 1);
-            ptx::mbar_init(sh.acc0 + 8 * i, 1);
+            ptx::mbar_init(sh.loadA0 + 8 * i, 1);
+            ptx::mbar_init(sh.loadB0 + 8 * i, 1);
+            ptx::mbar_init(sh.freeA0 + 8 * i, 1);
+            ptx::mbar_init(sh.freeB0 + 8 * i, 1);
         }
         ptx::mbar_init(sh.first, 1);
         ptx::mbar_init(sh.sfull, 1);
@@ -225,17 +240,26 @@ __device__ __forceinline__ uint32_t bwd_setup(uint8_t *smem_raw, uint32_t &base,
     return *tmem_holder;
 }
 
-// Teardown: the MMA thread (128) waits for all its MMAs and drains the TMA
-// loads it issued (issued[s] loads on stage s), then warp 4 frees TMEM.
+// Loads the producer thread has issued, for the drain at the end.
+struct BwdLoads {
+    int a[2] = {0, 0}, b[2] = {0, 0};
+    bool first = false;
+};
+
+// Teardown: the MMA thread (128) waits for all its MMAs, the load thread
+// (160) for the copies it issued; then warp 4 frees TMEM.
 template <int D>
-__device__ __forceinline__ void bwd_teardown(uint32_t tmem, const BwdShared &sh, const int (&issued)[2],
-                                             bool first_issued) {
+__device__ __forceinline__ void bwd_teardown(uint32_t tmem, const BwdShared &sh, const BwdLoads &ld) {
     if (threadIdx.x == 128) {
         ptx::mma_commit(sh.done);
         wait_drain(sh.done, 0);
-        for (int s = 0; s < 2; ++s)
-            if (issued[s] > 0) wait_drain(sh.load0 + 8 * s, (issued[s] - 1) & 1);
-        if (first_issued) wait_drain(sh.first, 0);
+    }
+    if (threadIdx.x == 160) {
+        for (int s = 0; s < 2; ++s) {
+            if (ld.a[s] > 0) wait_drain(sh.loadA0 + 8 * s, (ld.a[s] - 1) & 1);
+            if (ld.b[s] > 0) wait_drain(sh.loadB0 + 8 * s, (ld.b[s] - 1) & 1);
+        }
+        if (ld.first) wait_drain(sh.first, 0);
     }
     ptx::tc_fence_before_sync();
     __syncthreads();
@@ -256,17 +280,19 @@ __device__ __forceinline__ void bwd_teardown(uint32_t tmem, const BwdShared &sh,
 // so phase A of step n+1 runs while dK(n) and dP^T(n+1) execute, and phase
 // B of step n while dV(n) and S^T(n+1) do.
 
+// Loads of the dK/dV kernel: K_j, V_j once; Q_i (tile A) and dO_i (tile B)
+// of query tile i_begin + n into stage n & 1, each refilled as soon as the
+// GEMMs reading it are done (dO after dV, Q after dK).
 template <int D>
-__device__ void dkdv_mma_role(const BwdParams &p, const BwdShared &sh, uint32_t tmem, uint32_t base, int j, int bh,
-                              int i_begin, int n_i, int (&issued)[2], bool &first_issued) {
+__device__ void dkdv_load_role(const BwdParams &p, const BwdShared &sh, uint32_t base, int j, int bh, int i_begin,
+                               int n_i, BwdLoads &ld) {
     using C = BwdConfig<D>;
     const uint32_t sK = base, sV = base + C::kTile;
     const uint32_t sQ[2] = {base + 2 * C::kTile, base + 3 * C::kTile};
     const uint32_t sdO[2] = {base + 4 * C::kTile, base + 5 * C::kTile};
-    const uint32_t tST = tmem + 0, tdPT = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
     constexpr int kChunks = D / 64;
     ptx::mbar_arrive_expect_tx(sh.first, 2 * C::kTile);
-    first_issued = true;
+    ld.first = true;
     {
         const uint64_t pol = ptx::l2_policy_evict_first();
         for (int c = 0; c < kChunks; ++c) {
@@ -275,23 +301,48 @@ __device__ void dkdv_mma_role(const BwdParams &p, const BwdShared &sh, uint32_t 
         }
     }
     for (int s = 0; s < 2 && s < n_i; ++s) {
-        bwd_load_pair(&p.tmQ, &p.tmdO, sQ[s], sdO[s], sh.load0 + 8 * s, (i_begin + s) * kBR, bh, kChunks, C::kTile);
-        ++issued[s];
+        bwd_load_tile(&p.tmQ, sQ[s], sh.loadA0 + 8 * s, (i_begin + s) * kBR, bh, kChunks, C::kTile);
+        ++ld.a[s];
+        bwd_load_tile(&p.tmdO, sdO[s], sh.loadB0 + 8 * s, (i_begin + s) * kBR, bh, kChunks, C::kTile);
+        ++ld.b[s];
     }
+    for (int n = 0; n + 2 < n_i; ++n) {
+        const int s = n & 1;
+        const uint32_t par = (n >> 1) & 1;
+        if (!wait_bar(sh.freeB0 + 8 * s, par, sh.abort_flag, 18, blockIdx.x, n)) return;
+        bwd_load_tile(&p.tmdO, sdO[s], sh.loadB0 + 8 * s, (i_begin + n + 2) * kBR, bh, kChunks, C::kTile);
+        ++ld.b[s];
+        if (!wait_bar(sh.freeA0 + 8 * s, par, sh.abort_flag, 18, blockIdx.x, n)) return;
+        bwd_load_tile(&p.tmQ, sQ[s], sh.loadA0 + 8 * s, (i_begin + n + 2) * kBR, bh, kChunks, C::kTile);
+        ++ld.a[s];
+    }
+}
+
+template <int D>
+__device__ void dkdv_mma_role(const BwdParams &p, const BwdShared &sh, uint32_t tmem, uint32_t base, int n_i) {
+    using C = BwdConfig<D>;
+    const uint32_t sK = base, sV = base + C::kTile;
+    const uint32_t sQ[2] = {base + 2 * C::kTile, base + 3 * C::kTile};
+    const uint32_t sdO[2] = {base + 4 * C::kTile, base + 5 * C::kTile};
+    const uint32_t tST = tmem + 0, tdPT = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
     if (!wait_bar(sh.first, 0, sh.abort_flag, 10, blockIdx.x, -1)) return;
-    if (!wait_bar(sh.load0, 0, sh.abort_flag, 10, blockIdx.x, 0)) return;
+    if (!wait_bar(sh.loadA0, 0, sh.abort_flag, 10, blockIdx.x, 0)) return;
     ptx::tc_fence_after_sync();
     issue_s<D>(tST, sK, sQ[0]);      // S^T(0) = K Q_0^T
     ptx::mma_commit(sh.sfull);
+    if (!wait_bar(sh.loadB0, 0, sh.abort_flag, 10, blockIdx.x, 0)) return;
+    ptx::tc_fence_after_sync();
     issue_s<D>(tdPT, sV, sdO[0]);    // dP^T(0) = V dO_0^T
     ptx::mma_commit(sh.dpfull);
     for (int n = 0; n < n_i; ++n) {
         const int s = n & 1;
+        const uint32_t next_par = ((n + 1) >> 1) & 1;
         if (!wait_bar(sh.pready, n & 1, sh.abort_flag, 11, blockIdx.x, n)) return;
         ptx::tc_fence_after_sync();
         issue_pv<D>(tdV, tST, sdO[s], n > 0);                 // dV += P^T dO_n
+        ptx::mma_commit(sh.freeB0 + 8 * s);                   // dO_n read for the last time
         if (n + 1 < n_i) {
-            if (!wait_bar(sh.load0 + 8 * (s ^ 1), ((n + 1) >> 1) & 1, sh.abort_flag, 12, blockIdx.x, n + 1)) return;
+            if (!wait_bar(sh.loadA0 + 8 * (s ^ 1), next_par, sh.abort_flag, 12, blockIdx.x, n + 1)) return;
             ptx::tc_fence_after_sync();
             issue_s<D>(tST, sK, sQ[s ^ 1]);                   // S^T(n+1)
             ptx::mma_commit(sh.sfull);
@@ -299,16 +350,12 @@ __device__ void dkdv_mma_role(const BwdParams &p, const BwdShared &sh, uint32_t 
         if (!wait_bar(sh.dsready, n & 1, sh.abort_flag, 13, blockIdx.x, n)) return;
         ptx::tc_fence_after_sync();
         issue_pv<D>(tdK, tdPT, sQ[s], n > 0);                 // dK += dS^T Q_n
-        ptx::mma_commit(sh.acc0 + 8 * s);                     // stage s read for the last time
+        ptx::mma_commit(sh.freeA0 + 8 * s);                   // Q_n read for the last time
         if (n + 1 < n_i) {
+            if (!wait_bar(sh.loadB0 + 8 * (s ^ 1), next_par, sh.abort_flag, 14, blockIdx.x, n + 1)) return;
+            ptx::tc_fence_after_sync();
             issue_s<D>(tdPT, sV, sdO[s ^ 1]);                 // dP^T(n+1)
             ptx::mma_commit(sh.dpfull);
-        }
-        if (n + 2 < n_i) {   // refill stage s once its readers are done
-            if (!wait_bar(sh.acc0 + 8 * s, (n >> 1) & 1, sh.abort_flag, 14, blockIdx.x, n)) return;
-            bwd_load_pair(&p.tmQ, &p.tmdO, sQ[s], sdO[s], sh.load0 + 8 * s, (i_begin + n + 2) * kBR, bh, kChunks,
-                          C::kTile);
-            ++issued[s];
         }
     }
 }
@@ -360,7 +407,7 @@ __device__ void dkdv_elementwise_role(const BwdParams &p, const BwdShared &sh, u
     if (!ptx::named_barrier_and(1, 128, ok)) return;
     // the last accumulation done: dV and scale * dK for this key
     const int s = (n_i - 1) & 1;
-    if (!wait_bar(sh.acc0 + 8 * s, ((n_i - 1) >> 1) & 1, sh.abort_flag, 17, blockIdx.x, n_i)) return;
+    if (!wait_bar(sh.freeA0 + 8 * s, ((n_i - 1) >> 1) & 1, sh.abort_flag, 17, blockIdx.x, n_i)) return;
     ptx::tc_fence_after_sync();
     const bool live = key < p.Nk;
     store_row_bf16<D>(tdV, 1.f, p.dV + out_row, live);
@@ -380,16 +427,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
     const int bh = blockIdx.x % p.BH;
     const int i_begin = p.causal ? j : 0;      // query tiles that can see key tile j
     const int n_i = p.Tr - i_begin;
-    int issued[2] = {0, 0};
-    bool first_issued = false;
+    BwdLoads ld;
     if (threadIdx.x < 128) {
         dkdv_elementwise_role<D>(p, sh, tmem, reinterpret_cast<float *>(base_ptr + C::kStatOffset), j, bh, i_begin,
                                  n_i);
     } else if (threadIdx.x == 128 && n_i > 0) {
-        dkdv_mma_role<D>(p, sh, tmem, base, j, bh, i_begin, n_i, issued, first_issued);
+        dkdv_mma_role<D>(p, sh, tmem, base, n_i);
+    } else if (threadIdx.x == 160 && n_i > 0) {
+        dkdv_load_role<D>(p, sh, base, j, bh, i_begin, n_i, ld);
     }
     __syncwarp();
-    bwd_teardown<D>(tmem, sh, issued, first_issued);
+    bwd_teardown<D>(tmem, sh, ld);
 }
 
 // --------------------------------------------------------------- dQ kernel
@@ -399,33 +447,60 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
 //   wait S(n) read -> S(n+1) = Q K_{n+1}^T   (S(n) is in the threads' registers)
 //   wait dS(n)     -> dQ += dS K_n;  dP(n+1) = dO V_{n+1}^T
 
+// Loads of the dQ kernel: Q_i, dO_i once; K_j (tile A) and V_j (tile B) of
+// key tile n into stage n & 1, each refilled once its GEMMs are done (V
+// after dP, K after dQ).
 template <int D>
-__device__ void dq_mma_role(const BwdParams &p, const BwdShared &sh, uint32_t tmem, uint32_t base, int i, int bh,
-                            int n_j, int (&issued)[2], bool &first_issued) {
+__device__ void dq_load_role(const BwdParams &p, const BwdShared &sh, uint32_t base, int i, int bh, int n_j,
+                             BwdLoads &ld) {
+    using C = BwdConfig<D>;
+    const uint32_t sQ = base, sdO = base + C::kTile;
+    const uint32_t sK[2] = {base + 2 * C::kTile, base + 3 * C::kTile};
+    const uint32_t sV[2] = {base + 4 * C::kTile, base + 5 * C::kTile};
+    constexpr int kChunks = D / 64;
+    bwd_load_pair(&p.tmQ, &p.tmdO, sQ, sdO, sh.first, i * kBR, bh, kChunks, C::kTile);
+    ld.first = true;
+    for (int s = 0; s < 2 && s < n_j; ++s) {
+        bwd_load_tile(&p.tmK, sK[s], sh.loadA0 + 8 * s, s * kBC, bh, kChunks, C::kTile);
+        ++ld.a[s];
+        bwd_load_tile(&p.tmV, sV[s], sh.loadB0 + 8 * s, s * kBC, bh, kChunks, C::kTile);
+        ++ld.b[s];
+    }
+    for (int n = 0; n + 2 < n_j; ++n) {
+        const int s = n & 1;
+        const uint32_t par = (n >> 1) & 1;
+        if (!wait_bar(sh.freeB0 + 8 * s, par, sh.abort_flag, 28, blockIdx.x, n)) return;
+        bwd_load_tile(&p.tmV, sV[s], sh.loadB0 + 8 * s, (n + 2) * kBC, bh, kChunks, C::kTile);
+        ++ld.b[s];
+        if (!wait_bar(sh.freeA0 + 8 * s, par, sh.abort_flag, 28, blockIdx.x, n)) return;
+        bwd_load_tile(&p.tmK, sK[s], sh.loadA0 + 8 * s, (n + 2) * kBC, bh, kChunks, C::kTile);
+        ++ld.a[s];
+    }
+}
+
+template <int D>
+__device__ void dq_mma_role(const BwdParams &p, const BwdShared &sh, uint32_t tmem, uint32_t base, int n_j) {
     using C = BwdConfig<D>;
     const uint32_t sQ = base, sdO = base + C::kTile;
     const uint32_t sK[2] = {base + 2 * C::kTile, base + 3 * C::kTile};
     const uint32_t sV[2] = {base + 4 * C::kTile, base + 5 * C::kTile};
     const uint32_t tS = tmem + 0, tdP = tmem + 128, tdQ = tmem + 256;
-    constexpr int kChunks = D / 64;
-    bwd_load_pair(&p.tmQ, &p.tmdO, sQ, sdO, sh.first, i * kBR, bh, kChunks, C::kTile);
-    first_issued = true;
-    for (int s = 0; s < 2 && s < n_j; ++s) {
-        bwd_load_pair(&p.tmK, &p.tmV, sK[s], sV[s], sh.load0 + 8 * s, s * kBC, bh, kChunks, C::kTile);
-        ++issued[s];
-    }
     if (!wait_bar(sh.first, 0, sh.abort_flag, 20, blockIdx.x, -1)) return;
-    if (!wait_bar(sh.load0, 0, sh.abort_flag, 20, blockIdx.x, 0)) return;
+    if (!wait_bar(sh.loadA0, 0, sh.abort_flag, 20, blockIdx.x, 0)) return;
     ptx::tc_fence_after_sync();
     issue_s<D>(tS, sQ, sK[0]);      // S(0) = Q K_0^T
     ptx::mma_commit(sh.sfull);
+    if (!wait_bar(sh.loadB0, 0, sh.abort_flag, 20, blockIdx.x, 0)) return;
+    ptx::tc_fence_after_sync();
     issue_s<D>(tdP, sdO, sV[0]);    // dP(0) = dO V_0^T
     ptx::mma_commit(sh.dpfull);
+    ptx::mma_commit(sh.freeB0);     // V_0 read for the last time
     for (int n = 0; n < n_j; ++n) {
         const int s = n & 1;
+        const uint32_t next_par = ((n + 1) >> 1) & 1;
         if (!wait_bar(sh.pready, n & 1, sh.abort_flag, 21, blockIdx.x, n)) return;
         if (n + 1 < n_j) {
-            if (!wait_bar(sh.load0 + 8 * (s ^ 1), ((n + 1) >> 1) & 1, sh.abort_flag, 22, blockIdx.x, n + 1)) return;
+            if (!wait_bar(sh.loadA0 + 8 * (s ^ 1), next_par, sh.abort_flag, 22, blockIdx.x, n + 1)) return;
             ptx::tc_fence_after_sync();
             issue_s<D>(tS, sQ, sK[s ^ 1]);                    // S(n+1)
             ptx::mma_commit(sh.sfull);
@@ -433,15 +508,13 @@ __device__ void dq_mma_role(const BwdParams &p, const BwdShared &sh, uint32_t tm
         if (!wait_bar(sh.dsready, n & 1, sh.abort_flag, 23, blockIdx.x, n)) return;
         ptx::tc_fence_after_sync();
         issue_pv<D>(tdQ, tdP, sK[s], n > 0);                  // dQ += dS K_n
+        ptx::mma_commit(sh.freeA0 + 8 * s);                   // K_n read for the last time
         if (n + 1 < n_j) {
+            if (!wait_bar(sh.loadB0 + 8 * (s ^ 1), next_par, sh.abort_flag, 24, blockIdx.x, n + 1)) return;
+            ptx::tc_fence_after_sync();
             issue_s<D>(tdP, sdO, sV[s ^ 1]);                  // dP(n+1)
             ptx::mma_commit(sh.dpfull);
-        }
-        ptx::mma_commit(sh.acc0 + 8 * s);                     // stage s read for the last time
-        if (n + 2 < n_j) {
-            if (!wait_bar(sh.acc0 + 8 * s, (n >> 1) & 1, sh.abort_flag, 24, blockIdx.x, n)) return;
-            bwd_load_pair(&p.tmK, &p.tmV, sK[s], sV[s], sh.load0 + 8 * s, (n + 2) * kBC, bh, kChunks, C::kTile);
-            ++issued[s];
+            ptx::mma_commit(sh.freeB0 + 8 * (s ^ 1));         // V_{n+1} read for the last time
         }
     }
 }
@@ -476,7 +549,7 @@ __device__ void dq_elementwise_role(const BwdParams &p, const BwdShared &sh, uin
         tmem_stores_then_arrive(sh.dsready);
     }
     const int s = (n_j - 1) & 1;
-    if (!wait_bar(sh.acc0 + 8 * s, ((n_j - 1) >> 1) & 1, sh.abort_flag, 27, blockIdx.x, n_j)) return;
+    if (!wait_bar(sh.freeA0 + 8 * s, ((n_j - 1) >> 1) & 1, sh.abort_flag, 27, blockIdx.x, n_j)) return;
     ptx::tc_fence_after_sync();
     store_row_bf16<D>(tdQ, p.scale, p.dQ + (static_cast<size_t>(bh) * p.Nq + q) * D, qlive);
 }
@@ -496,12 +569,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
         const int q_end = min(p.Nq, (i + 1) * kBR);
         n_j = min(p.Tc, (q_end - 1) / kBC + 1);
     }
-    int issued[2] = {0, 0};
-    bool first_issued = false;
+    BwdLoads ld;
     if (threadIdx.x < 128) dq_elementwise_role<D>(p, sh, tmem, i, bh, n_j);
-    else if (threadIdx.x == 128) dq_mma_role<D>(p, sh, tmem, base, i, bh, n_j, issued, first_issued);
+    else if (threadIdx.x == 128) dq_mma_role<D>(p, sh, tmem, base, n_j);
+    else if (threadIdx.x == 160) dq_load_role<D>(p, sh, base, i, bh, n_j, ld);
     __syncwarp();
-    bwd_teardown<D>(tmem, sh, issued, first_issued);
+    bwd_teardown<D>(tmem, sh, ld);
 }
 
 }  // namespace fa
