@@ -664,7 +664,8 @@ extern "C" fa_status fa_check_device_status(fa_stream_t stream) {
     if (status == 0) return FA_OK;
     const unsigned int zero = 0;
     if (cudaMemcpyToSymbol(fa::g_fa_status, &zero, sizeof zero) != cudaSuccess) return FA_ERR_CUDA;
-    return FA_ERR_TIMEOUT;
+    // bit 2: a backward kernel got a shared-memory base it could not align and did nothing
+    return (status & 4u) ? FA_ERR_CUDA : FA_ERR_TIMEOUT;
 }
 
 extern "C" const char *fa_status_string(fa_status s) {

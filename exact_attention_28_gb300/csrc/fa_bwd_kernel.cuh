@@ -39,16 +39,26 @@ struct BwdParams {
     float scale;
 };
 
+// Streamed tiles: A (Q in dK/dV, K in dQ) has three slots, B (dO, V) two.
+// A is read last by the step's final GEMM, so with two slots its refill
+// could start only about one step before it is needed again.
+constexpr int kSlotsA = 3, kSlotsB = 2;
+
 template <int D>
 struct BwdConfig {
     static constexpr int kTile = 128 * D * 2;            // one [128][D] bf16 tile
-    // dK/dV kernel: K_j, V_j resident; Q_i, dO_i double-buffered
-    // dQ kernel:    Q_i, dO_i resident; K_j, V_j double-buffered
-    static constexpr int kTileBytes = 6 * kTile;
+    // dK/dV kernel: K_j, V_j resident; Q_i in 3 slots, dO_i in 2
+    // dQ kernel:    Q_i, dO_i resident; K_j in 3 slots, V_j in 2
+    static constexpr int kTileBytes = (2 + kSlotsA + kSlotsB) * kTile;
     static constexpr int kStatOffset = kTileBytes;       // 2 stages x (lse2[128], d[128]) fp32
     static constexpr int kBarOffset = kStatOffset + 2 * 2 * 128 * 4;
-    static constexpr int kSmemBytes = kBarOffset + 128 + 1024;
-    static_assert(kSmemBytes <= 232448, "shared memory");
+    static constexpr int kBarBytes = 160;
+    static constexpr int kUsed = kBarOffset + kBarBytes;
+    // room to align the dynamic shared memory to 1024 bytes (the kernel checks
+    // the base it gets against this slack)
+    static constexpr int kSmemBytes = kUsed + 1024 <= 232448 ? kUsed + 1024 : 232448;
+    static constexpr int kSlack = kSmemBytes - kUsed;
+    static_assert(kSlack >= 512, "shared memory");
     static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -76,11 +86,11 @@ __global__ void __launch_bounds__(256) fa_bwd_dot_kernel(const __nv_bfloat16 *__
 // ------------------------------------------------------------------ shared
 
 // Barriers of both kernels (one arrival unless noted).
-// A stage holds two streamed tiles, A and B: Q and dO in the dK/dV kernel,
-// K and V in the dQ kernel.
+// Streamed tiles A and B: Q and dO in the dK/dV kernel, K and V in the dQ
+// kernel; step n uses A slot n % 3 and B slot n % 2.
 struct BwdShared {
-    uint32_t loadA0, loadB0;   // + 8 * stage: the tile landed
-    uint32_t freeA0, freeB0;   // + 8 * stage: the last GEMM reading the tile completed
+    uint32_t loadA0, loadB0;   // + 8 * slot: the tile landed
+    uint32_t freeA0, freeB0;   // + 8 * slot: the last GEMM reading the tile completed
     uint32_t first;     // the resident pair of tiles landed
     uint32_t sfull;     // the score GEMM of the current step completed
     uint32_t dpfull;    // the dP GEMM of the current step completed
@@ -195,30 +205,41 @@ __device__ __forceinline__ void bwd_phase_b(const float (&pv)[128], uint32_t tdP
 }
 
 // Set-up of both kernels: smem carve-up, barriers, TMEM allocation by warp 4.
+// Returns false (on every thread, before anything else) when the dynamic
+// shared memory base leaves less than the configured slack for 1024-byte
+// alignment; the status word then gets bit 2 and the CTA does nothing.
 template <int D>
-__device__ __forceinline__ uint32_t bwd_setup(uint8_t *smem_raw, uint32_t &base, uint8_t *&base_ptr, BwdShared &sh) {
+__device__ __forceinline__ bool bwd_setup(uint8_t *smem_raw, uint32_t &base, uint8_t *&base_ptr, BwdShared &sh,
+                                          uint32_t &tmem) {
     using C = BwdConfig<D>;
     const uint32_t raw = ptx::smem_addr(smem_raw);
     base = (raw + 1023u) & ~1023u;
+    if (base - raw > static_cast<uint32_t>(C::kSlack)) {
+        if (threadIdx.x == 0) atomicOr(&g_fa_status, 4u);
+        return false;
+    }
     base_ptr = smem_raw + (base - raw);
     const uint32_t bars = base + C::kBarOffset;
-    sh.loadA0 = bars + 0;     // 2
-    sh.loadB0 = bars + 16;    // 2
-    sh.freeA0 = bars + 32;    // 2
-    sh.freeB0 = bars + 48;    // 2
-    sh.first = bars + 64;
-    sh.sfull = bars + 72;
-    sh.dpfull = bars + 80;
-    sh.pready = bars + 88;
-    sh.dsready = bars + 96;
-    sh.done = bars + 104;
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(base_ptr + C::kBarOffset + 112);
-    sh.abort_flag = reinterpret_cast<volatile int *>(base_ptr + C::kBarOffset + 116);
+    sh.loadA0 = bars + 0;     // kSlotsA
+    sh.loadB0 = bars + 24;    // kSlotsB
+    sh.freeA0 = bars + 40;    // kSlotsA
+    sh.freeB0 = bars + 64;    // kSlotsB
+    sh.first = bars + 80;
+    sh.sfull = bars + 88;
+    sh.dpfull = bars + 96;
+    sh.pready = bars + 104;
+    sh.dsready = bars + 112;
+    sh.done = bars + 120;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(base_ptr + C::kBarOffset + 128);
+    sh.abort_flag = reinterpret_cast<volatile int *>(base_ptr + C::kBarOffset + 132);
+    static_assert(136 <= C::kBarBytes, "barrier block");
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kSlotsA; ++i) {
             ptx::mbar_init(sh.loadA0 + 8 * i, 1);
-            ptx::mbar_init(sh.loadB0 + 8 * i, 1);
             ptx::mbar_init(sh.freeA0 + 8 * i, 1);
+        }
+        for (int i = 0; i < kSlotsB; ++i) {
+            ptx::mbar_init(sh.loadB0 + 8 * i, 1);
             ptx::mbar_init(sh.freeB0 + 8 * i, 1);
         }
         ptx::mbar_init(sh.first, 1);
@@ -237,12 +258,13 @@ __device__ __forceinline__ uint32_t bwd_setup(uint8_t *smem_raw, uint32_t &base,
     ptx::tc_fence_before_sync();
     __syncthreads();
     ptx::tc_fence_after_sync();
-    return *tmem_holder;
+    tmem = *tmem_holder;
+    return true;
 }
 
 // Loads the producer thread has issued, for the drain at the end.
 struct BwdLoads {
-    int a[2] = {0, 0}, b[2] = {0, 0};
+    int a[kSlotsA] = {0, 0, 0}, b[kSlotsB] = {0, 0};
     bool first = false;
 };
 
@@ -255,10 +277,10 @@ __device__ __forceinline__ void bwd_teardown(uint32_t tmem, const BwdShared &sh,
         wait_drain(sh.done, 0);
     }
     if (threadIdx.x == 160) {
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kSlotsA; ++s)
             if (ld.a[s] > 0) wait_drain(sh.loadA0 + 8 * s, (ld.a[s] - 1) & 1);
+        for (int s = 0; s < kSlotsB; ++s)
             if (ld.b[s] > 0) wait_drain(sh.loadB0 + 8 * s, (ld.b[s] - 1) & 1);
-        }
         if (ld.first) wait_drain(sh.first, 0);
     }
     ptx::tc_fence_before_sync();
@@ -280,16 +302,15 @@ __device__ __forceinline__ void bwd_teardown(uint32_t tmem, const BwdShared &sh,
 // so phase A of step n+1 runs while dK(n) and dP^T(n+1) execute, and phase
 // B of step n while dV(n) and S^T(n+1) do.
 
-// Loads of the dK/dV kernel: K_j, V_j once; Q_i (tile A) and dO_i (tile B)
-// of query tile i_begin + n into stage n & 1, each refilled as soon as the
-// GEMMs reading it are done (dO after dV, Q after dK).
+// Loads of the dK/dV kernel: K_j, V_j once; Q_i (tile A, slot n % 3) and
+// dO_i (tile B, slot n % 2) of query tile i_begin + n, each refilled as soon
+// as the GEMMs reading it are done (dO after dV, Q after dK).
 template <int D>
 __device__ void dkdv_load_role(const BwdParams &p, const BwdShared &sh, uint32_t base, int j, int bh, int i_begin,
                                int n_i, BwdLoads &ld) {
     using C = BwdConfig<D>;
     const uint32_t sK = base, sV = base + C::kTile;
-    const uint32_t sQ[2] = {base + 2 * C::kTile, base + 3 * C::kTile};
-    const uint32_t sdO[2] = {base + 4 * C::kTile, base + 5 * C::kTile};
+    const uint32_t sQ0 = base + 2 * C::kTile, sdO0 = base + (2 + kSlotsA) * C::kTile;
     constexpr int kChunks = D / 64;
     ptx::mbar_arrive_expect_tx(sh.first, 2 * C::kTile);
     ld.first = true;
@@ -300,21 +321,26 @@ __device__ void dkdv_load_role(const BwdParams &p, const BwdShared &sh, uint32_t
             ptx::tma_load_3d(sV + c * kChunkBytes, &p.tmV, sh.first, c * 64, j * kBC, bh, pol);
         }
     }
-    for (int s = 0; s < 2 && s < n_i; ++s) {
-        bwd_load_tile(&p.tmQ, sQ[s], sh.loadA0 + 8 * s, (i_begin + s) * kBR, bh, kChunks, C::kTile);
-        ++ld.a[s];
-        bwd_load_tile(&p.tmdO, sdO[s], sh.loadB0 + 8 * s, (i_begin + s) * kBR, bh, kChunks, C::kTile);
-        ++ld.b[s];
+    for (int n = 0; n < kSlotsA && n < n_i; ++n) {
+        bwd_load_tile(&p.tmQ, sQ0 + n * C::kTile, sh.loadA0 + 8 * n, (i_begin + n) * kBR, bh, kChunks, C::kTile);
+        ++ld.a[n];
     }
-    for (int n = 0; n + 2 < n_i; ++n) {
-        const int s = n & 1;
-        const uint32_t par = (n >> 1) & 1;
-        if (!wait_bar(sh.freeB0 + 8 * s, par, sh.abort_flag, 18, blockIdx.x, n)) return;
-        bwd_load_tile(&p.tmdO, sdO[s], sh.loadB0 + 8 * s, (i_begin + n + 2) * kBR, bh, kChunks, C::kTile);
-        ++ld.b[s];
-        if (!wait_bar(sh.freeA0 + 8 * s, par, sh.abort_flag, 18, blockIdx.x, n)) return;
-        bwd_load_tile(&p.tmQ, sQ[s], sh.loadA0 + 8 * s, (i_begin + n + 2) * kBR, bh, kChunks, C::kTile);
-        ++ld.a[s];
+    for (int n = 0; n < kSlotsB && n < n_i; ++n) {
+        bwd_load_tile(&p.tmdO, sdO0 + n * C::kTile, sh.loadB0 + 8 * n, (i_begin + n) * kBR, bh, kChunks, C::kTile);
+        ++ld.b[n];
+    }
+    for (int n = 0; n + kSlotsB < n_i; ++n) {
+        const int a = n % kSlotsA, b = n % kSlotsB;
+        if (!wait_bar(sh.freeB0 + 8 * b, (n / kSlotsB) & 1, sh.abort_flag, 18, blockIdx.x, n)) return;
+        bwd_load_tile(&p.tmdO, sdO0 + b * C::kTile, sh.loadB0 + 8 * b, (i_begin + n + kSlotsB) * kBR, bh, kChunks,
+                      C::kTile);
+        ++ld.b[b];
+        if (n + kSlotsA < n_i) {
+            if (!wait_bar(sh.freeA0 + 8 * a, (n / kSlotsA) & 1, sh.abort_flag, 18, blockIdx.x, n)) return;
+            bwd_load_tile(&p.tmQ, sQ0 + a * C::kTile, sh.loadA0 + 8 * a, (i_begin + n + kSlotsA) * kBR, bh, kChunks,
+                          C::kTile);
+            ++ld.a[a];
+        }
     }
 }
 
@@ -322,39 +348,38 @@ template <int D>
 __device__ void dkdv_mma_role(const BwdParams &p, const BwdShared &sh, uint32_t tmem, uint32_t base, int n_i) {
     using C = BwdConfig<D>;
     const uint32_t sK = base, sV = base + C::kTile;
-    const uint32_t sQ[2] = {base + 2 * C::kTile, base + 3 * C::kTile};
-    const uint32_t sdO[2] = {base + 4 * C::kTile, base + 5 * C::kTile};
+    const uint32_t sQ0 = base + 2 * C::kTile, sdO0 = base + (2 + kSlotsA) * C::kTile;
     const uint32_t tST = tmem + 0, tdPT = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
     if (!wait_bar(sh.first, 0, sh.abort_flag, 10, blockIdx.x, -1)) return;
     if (!wait_bar(sh.loadA0, 0, sh.abort_flag, 10, blockIdx.x, 0)) return;
     ptx::tc_fence_after_sync();
-    issue_s<D>(tST, sK, sQ[0]);      // S^T(0) = K Q_0^T
+    issue_s<D>(tST, sK, sQ0);        // S^T(0) = K Q_0^T
     ptx::mma_commit(sh.sfull);
     if (!wait_bar(sh.loadB0, 0, sh.abort_flag, 10, blockIdx.x, 0)) return;
     ptx::tc_fence_after_sync();
-    issue_s<D>(tdPT, sV, sdO[0]);    // dP^T(0) = V dO_0^T
+    issue_s<D>(tdPT, sV, sdO0);      // dP^T(0) = V dO_0^T
     ptx::mma_commit(sh.dpfull);
     for (int n = 0; n < n_i; ++n) {
-        const int s = n & 1;
-        const uint32_t next_par = ((n + 1) >> 1) & 1;
+        const int a = n % kSlotsA, b = n % kSlotsB;
+        const int an = (n + 1) % kSlotsA, bn = (n + 1) % kSlotsB;
         if (!wait_bar(sh.pready, n & 1, sh.abort_flag, 11, blockIdx.x, n)) return;
         ptx::tc_fence_after_sync();
-        issue_pv<D>(tdV, tST, sdO[s], n > 0);                 // dV += P^T dO_n
-        ptx::mma_commit(sh.freeB0 + 8 * s);                   // dO_n read for the last time
+        issue_pv<D>(tdV, tST, sdO0 + b * C::kTile, n > 0);    // dV += P^T dO_n
+        ptx::mma_commit(sh.freeB0 + 8 * b);                   // dO_n read for the last time
         if (n + 1 < n_i) {
-            if (!wait_bar(sh.loadA0 + 8 * (s ^ 1), next_par, sh.abort_flag, 12, blockIdx.x, n + 1)) return;
+            if (!wait_bar(sh.loadA0 + 8 * an, ((n + 1) / kSlotsA) & 1, sh.abort_flag, 12, blockIdx.x, n + 1)) return;
             ptx::tc_fence_after_sync();
-            issue_s<D>(tST, sK, sQ[s ^ 1]);                   // S^T(n+1)
+            issue_s<D>(tST, sK, sQ0 + an * C::kTile);         // S^T(n+1)
             ptx::mma_commit(sh.sfull);
         }
         if (!wait_bar(sh.dsready, n & 1, sh.abort_flag, 13, blockIdx.x, n)) return;
         ptx::tc_fence_after_sync();
-        issue_pv<D>(tdK, tdPT, sQ[s], n > 0);                 // dK += dS^T Q_n
-        ptx::mma_commit(sh.freeA0 + 8 * s);                   // Q_n read for the last time
+        issue_pv<D>(tdK, tdPT, sQ0 + a * C::kTile, n > 0);    // dK += dS^T Q_n
+        ptx::mma_commit(sh.freeA0 + 8 * a);                   // Q_n read for the last time
         if (n + 1 < n_i) {
-            if (!wait_bar(sh.loadB0 + 8 * (s ^ 1), next_par, sh.abort_flag, 14, blockIdx.x, n + 1)) return;
+            if (!wait_bar(sh.loadB0 + 8 * bn, ((n + 1) / kSlotsB) & 1, sh.abort_flag, 14, blockIdx.x, n + 1)) return;
             ptx::tc_fence_after_sync();
-            issue_s<D>(tdPT, sV, sdO[s ^ 1]);                 // dP^T(n+1)
+            issue_s<D>(tdPT, sV, sdO0 + bn * C::kTile);       // dP^T(n+1)
             ptx::mma_commit(sh.dpfull);
         }
     }
@@ -406,8 +431,8 @@ __device__ void dkdv_elementwise_role(const BwdParams &p, const BwdShared &sh, u
     }
     if (!ptx::named_barrier_and(1, 128, ok)) return;
     // the last accumulation done: dV and scale * dK for this key
-    const int s = (n_i - 1) & 1;
-    if (!wait_bar(sh.freeA0 + 8 * s, ((n_i - 1) >> 1) & 1, sh.abort_flag, 17, blockIdx.x, n_i)) return;
+    const int a_last = (n_i - 1) % kSlotsA;
+    if (!wait_bar(sh.freeA0 + 8 * a_last, ((n_i - 1) / kSlotsA) & 1, sh.abort_flag, 17, blockIdx.x, n_i)) return;
     ptx::tc_fence_after_sync();
     const bool live = key < p.Nk;
     store_row_bf16<D>(tdV, 1.f, p.dV + out_row, live);
@@ -421,7 +446,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
     uint32_t base;
     uint8_t *base_ptr;
     BwdShared sh;
-    const uint32_t tmem = bwd_setup<D>(smem_raw, base, base_ptr, sh);
+    uint32_t tmem;
+    if (!bwd_setup<D>(smem_raw, base, base_ptr, sh, tmem)) return;
     // heavy tiles (small j under the causal mask) get the low block indices
     const int j = blockIdx.x / p.BH;
     const int bh = blockIdx.x % p.BH;
@@ -447,34 +473,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
 //   wait S(n) read -> S(n+1) = Q K_{n+1}^T   (S(n) is in the threads' registers)
 //   wait dS(n)     -> dQ += dS K_n;  dP(n+1) = dO V_{n+1}^T
 
-// Loads of the dQ kernel: Q_i, dO_i once; K_j (tile A) and V_j (tile B) of
-// key tile n into stage n & 1, each refilled once its GEMMs are done (V
-// after dP, K after dQ).
+// Loads of the dQ kernel: Q_i, dO_i once; K_j (tile A, slot n % 3) and V_j
+// (tile B, slot n % 2) of key tile n, each refilled once its GEMMs are done
+// (V after dP, K after dQ).
 template <int D>
 __device__ void dq_load_role(const BwdParams &p, const BwdShared &sh, uint32_t base, int i, int bh, int n_j,
                              BwdLoads &ld) {
     using C = BwdConfig<D>;
     const uint32_t sQ = base, sdO = base + C::kTile;
-    const uint32_t sK[2] = {base + 2 * C::kTile, base + 3 * C::kTile};
-    const uint32_t sV[2] = {base + 4 * C::kTile, base + 5 * C::kTile};
+    const uint32_t sK0 = base + 2 * C::kTile, sV0 = base + (2 + kSlotsA) * C::kTile;
     constexpr int kChunks = D / 64;
     bwd_load_pair(&p.tmQ, &p.tmdO, sQ, sdO, sh.first, i * kBR, bh, kChunks, C::kTile);
     ld.first = true;
-    for (int s = 0; s < 2 && s < n_j; ++s) {
-        bwd_load_tile(&p.tmK, sK[s], sh.loadA0 + 8 * s, s * kBC, bh, kChunks, C::kTile);
-        ++ld.a[s];
-        bwd_load_tile(&p.tmV, sV[s], sh.loadB0 + 8 * s, s * kBC, bh, kChunks, C::kTile);
-        ++ld.b[s];
+    for (int n = 0; n < kSlotsA && n < n_j; ++n) {
+        bwd_load_tile(&p.tmK, sK0 + n * C::kTile, sh.loadA0 + 8 * n, n * kBC, bh, kChunks, C::kTile);
+        ++ld.a[n];
     }
-    for (int n = 0; n + 2 < n_j; ++n) {
-        const int s = n & 1;
-        const uint32_t par = (n >> 1) & 1;
-        if (!wait_bar(sh.freeB0 + 8 * s, par, sh.abort_flag, 28, blockIdx.x, n)) return;
-        bwd_load_tile(&p.tmV, sV[s], sh.loadB0 + 8 * s, (n + 2) * kBC, bh, kChunks, C::kTile);
-        ++ld.b[s];
-        if (!wait_bar(sh.freeA0 + 8 * s, par, sh.abort_flag, 28, blockIdx.x, n)) return;
-        bwd_load_tile(&p.tmK, sK[s], sh.loadA0 + 8 * s, (n + 2) * kBC, bh, kChunks, C::kTile);
-        ++ld.a[s];
+    for (int n = 0; n < kSlotsB && n < n_j; ++n) {
+        bwd_load_tile(&p.tmV, sV0 + n * C::kTile, sh.loadB0 + 8 * n, n * kBC, bh, kChunks, C::kTile);
+        ++ld.b[n];
+    }
+    for (int n = 0; n + kSlotsB < n_j; ++n) {
+        const int a = n % kSlotsA, b = n % kSlotsB;
+        if (!wait_bar(sh.freeB0 + 8 * b, (n / kSlotsB) & 1, sh.abort_flag, 28, blockIdx.x, n)) return;
+        bwd_load_tile(&p.tmV, sV0 + b * C::kTile, sh.loadB0 + 8 * b, (n + kSlotsB) * kBC, bh, kChunks, C::kTile);
+        ++ld.b[b];
+        if (n + kSlotsA < n_j) {
+            if (!wait_bar(sh.freeA0 + 8 * a, (n / kSlotsA) & 1, sh.abort_flag, 28, blockIdx.x, n)) return;
+            bwd_load_tile(&p.tmK, sK0 + a * C::kTile, sh.loadA0 + 8 * a, (n + kSlotsA) * kBC, bh, kChunks, C::kTile);
+            ++ld.a[a];
+        }
     }
 }
 
@@ -482,39 +510,38 @@ template <int D>
 __device__ void dq_mma_role(const BwdParams &p, const BwdShared &sh, uint32_t tmem, uint32_t base, int n_j) {
     using C = BwdConfig<D>;
     const uint32_t sQ = base, sdO = base + C::kTile;
-    const uint32_t sK[2] = {base + 2 * C::kTile, base + 3 * C::kTile};
-    const uint32_t sV[2] = {base + 4 * C::kTile, base + 5 * C::kTile};
+    const uint32_t sK0 = base + 2 * C::kTile, sV0 = base + (2 + kSlotsA) * C::kTile;
     const uint32_t tS = tmem + 0, tdP = tmem + 128, tdQ = tmem + 256;
     if (!wait_bar(sh.first, 0, sh.abort_flag, 20, blockIdx.x, -1)) return;
     if (!wait_bar(sh.loadA0, 0, sh.abort_flag, 20, blockIdx.x, 0)) return;
     ptx::tc_fence_after_sync();
-    issue_s<D>(tS, sQ, sK[0]);      // S(0) = Q K_0^T
+    issue_s<D>(tS, sQ, sK0);        // S(0) = Q K_0^T
     ptx::mma_commit(sh.sfull);
     if (!wait_bar(sh.loadB0, 0, sh.abort_flag, 20, blockIdx.x, 0)) return;
     ptx::tc_fence_after_sync();
-    issue_s<D>(tdP, sdO, sV[0]);    // dP(0) = dO V_0^T
+    issue_s<D>(tdP, sdO, sV0);      // dP(0) = dO V_0^T
     ptx::mma_commit(sh.dpfull);
     ptx::mma_commit(sh.freeB0);     // V_0 read for the last time
     for (int n = 0; n < n_j; ++n) {
-        const int s = n & 1;
-        const uint32_t next_par = ((n + 1) >> 1) & 1;
+        const int a = n % kSlotsA;
+        const int an = (n + 1) % kSlotsA, bn = (n + 1) % kSlotsB;
         if (!wait_bar(sh.pready, n & 1, sh.abort_flag, 21, blockIdx.x, n)) return;
         if (n + 1 < n_j) {
-            if (!wait_bar(sh.loadA0 + 8 * (s ^ 1), next_par, sh.abort_flag, 22, blockIdx.x, n + 1)) return;
+            if (!wait_bar(sh.loadA0 + 8 * an, ((n + 1) / kSlotsA) & 1, sh.abort_flag, 22, blockIdx.x, n + 1)) return;
             ptx::tc_fence_after_sync();
-            issue_s<D>(tS, sQ, sK[s ^ 1]);                    // S(n+1)
+            issue_s<D>(tS, sQ, sK0 + an * C::kTile);          // S(n+1)
             ptx::mma_commit(sh.sfull);
         }
         if (!wait_bar(sh.dsready, n & 1, sh.abort_flag, 23, blockIdx.x, n)) return;
         ptx::tc_fence_after_sync();
-        issue_pv<D>(tdQ, tdP, sK[s], n > 0);                  // dQ += dS K_n
-        ptx::mma_commit(sh.freeA0 + 8 * s);                   // K_n read for the last time
+        issue_pv<D>(tdQ, tdP, sK0 + a * C::kTile, n > 0);     // dQ += dS K_n
+        ptx::mma_commit(sh.freeA0 + 8 * a);                   // K_n read for the last time
         if (n + 1 < n_j) {
-            if (!wait_bar(sh.loadB0 + 8 * (s ^ 1), next_par, sh.abort_flag, 24, blockIdx.x, n + 1)) return;
+            if (!wait_bar(sh.loadB0 + 8 * bn, ((n + 1) / kSlotsB) & 1, sh.abort_flag, 24, blockIdx.x, n + 1)) return;
             ptx::tc_fence_after_sync();
-            issue_s<D>(tdP, sdO, sV[s ^ 1]);                  // dP(n+1)
+            issue_s<D>(tdP, sdO, sV0 + bn * C::kTile);        // dP(n+1)
             ptx::mma_commit(sh.dpfull);
-            ptx::mma_commit(sh.freeB0 + 8 * (s ^ 1));         // V_{n+1} read for the last time
+            ptx::mma_commit(sh.freeB0 + 8 * bn);              // V_{n+1} read for the last time
         }
     }
 }
@@ -548,8 +575,8 @@ __device__ void dq_elementwise_role(const BwdParams &p, const BwdShared &sh, uin
         bwd_phase_b<false>(pv, tdP, nullptr, row_d);
         tmem_stores_then_arrive(sh.dsready);
     }
-    const int s = (n_j - 1) & 1;
-    if (!wait_bar(sh.freeA0 + 8 * s, ((n_j - 1) >> 1) & 1, sh.abort_flag, 27, blockIdx.x, n_j)) return;
+    const int a_last = (n_j - 1) % kSlotsA;
+    if (!wait_bar(sh.freeA0 + 8 * a_last, ((n_j - 1) / kSlotsA) & 1, sh.abort_flag, 27, blockIdx.x, n_j)) return;
     ptx::tc_fence_after_sync();
     store_row_bf16<D>(tdQ, p.scale, p.dQ + (static_cast<size_t>(bh) * p.Nq + q) * D, qlive);
 }
@@ -560,7 +587,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
     uint32_t base;
     uint8_t *base_ptr;
     BwdShared sh;
-    const uint32_t tmem = bwd_setup<D>(smem_raw, base, base_ptr, sh);
+    uint32_t tmem;
+    if (!bwd_setup<D>(smem_raw, base, base_ptr, sh, tmem)) return;
     // heavy tiles (large i under the causal mask) get the low block indices
     const int i = p.causal ? (p.Tr - 1 - blockIdx.x / p.BH) : blockIdx.x / p.BH;
     const int bh = blockIdx.x % p.BH;

@@ -89,7 +89,8 @@ fa_status fa_fwd_host(const void *hQ, const void *hK, const void *hV, void *hO, 
  * fa_check_device_status -- synchronises `stream`, then reads and clears the
  * device status word that kernels of this library set when one of their
  * bounded waits expires.  Returns FA_OK, FA_ERR_TIMEOUT, or FA_ERR_CUDA if the
- * synchronisation itself failed.
+ * synchronisation itself failed or a backward kernel was given a shared-memory
+ * base it could not align (it then computes nothing).
  */
 fa_status fa_check_device_status(fa_stream_t stream);
 
