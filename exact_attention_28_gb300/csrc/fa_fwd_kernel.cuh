@@ -298,6 +298,9 @@ struct Shared {
     uint32_t q_full, q_empty;
     uint32_t kv_full0, kv_empty0;  // + 8 * slot
     uint32_t s_full0, p_full0, o_full0;  // + 8 * tile
+    // single-tile items: S alternates between the two tiles' S regions;
+    // s_alt marks S ready in the second one, pv_done each P V but the last
+    uint32_t s_alt, pv_done;
     uint32_t done;
     volatile int *abort_flag;
 };
@@ -479,6 +482,45 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
         ptx::tc_fence_after_sync();
         if (nkv <= kv0) {   // an empty key slice: release Q and move on
             ptx::mma_commit(sh.q_empty);
+            continue;
+        }
+
+        if (item.ntiles == 1) {
+            // One query tile: S alternates between the two S regions, so S(j+1)
+            // is computed while the softmax works on S(j), and only P(j) V_j
+            // lies between two softmax steps.  Ring index of K(j) is
+            // b0 + 2 (j - kv0), of V(j) one more.
+            const uint32_t b0 = it;
+            auto ring_bar = [&](uint32_t idx) { return sh.kv_full0 + 8 * (idx % C::kSlots); };
+            auto ring_tile = [&](uint32_t idx) { return smem_ring + (idx % C::kSlots) * C::kKVTileBytes; };
+            auto issue_s_buf = [&](int jj) -> bool {   // S(jj) into buffer (jj - kv0) & 1
+                const uint32_t ki = b0 + 2 * (jj - kv0);
+                if (!wait_bar(ring_bar(ki), (ki / C::kSlots) & 1, sh.abort_flag, 1, w, jj)) return false;
+                ptx::tc_fence_after_sync();
+                const int buf = (jj - kv0) & 1;
+                issue_s<D, F8>(tS[buf], sQ[0], ring_tile(ki));
+                ptx::mma_commit(buf ? sh.s_alt : sh.s_full0);
+                ptx::mma_commit(sh.kv_empty0 + 8 * (ki % C::kSlots));
+                return true;
+            };
+            if (!issue_s_buf(kv0)) return;
+            if (kv0 + 1 < nk0 && !issue_s_buf(kv0 + 1)) return;
+            if (nk0 <= kv0 + 2) ptx::mma_commit(sh.q_empty);   // every S of the item issued
+            for (int j = kv0; j < nk0; ++j) {
+                const uint32_t vi = b0 + 2 * (j - kv0) + 1;
+                if (!wait_bar(ring_bar(vi), (vi / C::kSlots) & 1, sh.abort_flag, 1, w, j)) return;
+                if (!wait_bar(sh.p_full0, p_phase[0], sh.abort_flag, 1, w, j)) return;
+                p_phase[0] ^= 1u;
+                ptx::tc_fence_after_sync();
+                issue_pv<D, F8>(tO[0], tS[(j - kv0) & 1], ring_tile(vi), j > kv0);
+                ptx::mma_commit(j == nk0 - 1 ? sh.o_full0 : sh.pv_done);
+                ptx::mma_commit(sh.kv_empty0 + 8 * (vi % C::kSlots));
+                if (j + 2 < nk0) {
+                    if (!issue_s_buf(j + 2)) return;
+                    if (j + 3 == nk0) ptx::mma_commit(sh.q_empty);
+                }
+            }
+            it = b0 + 2 * (nk0 - kv0);
             continue;
         }
 
@@ -664,6 +706,7 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
     [[maybe_unused]] const int page_rows = p.block_size < kBC ? p.block_size : kBC;
     [[maybe_unused]] const int page_shift = (MODE & kPaged) != 0 ? 31 - __clz(page_rows) : 0;
     uint32_t s_phase = 0, o_phase = 0;
+    uint32_t sa_phase = 0, pv_phase = 0;   // single-tile items (tile 0 only)
 
     for (int k = 0;; ++k) {
         const int w = item_of_round(p, k);
@@ -688,6 +731,7 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
             continue;
         }
         const int key_lim = p.causal ? min(item.seq_len, qg + 1 + item.q_shift) : item.seq_len;
+        const bool single = item.ntiles == 1;
         [[maybe_unused]] float out_scale = 1.f;   // E4M3: V's descale
         if constexpr (F8) {
             // scores of the codes times descale_q * descale_k; kept a normal
@@ -708,11 +752,19 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
             [[maybe_unused]] int box_page = 0;
             if constexpr ((MODE & kPaged) != 0)
                 if (lane * page_rows < kBC) box_page = page_of_box(p, item.bh / p.H, j, lane, page_rows);
-            if (!wait_bar(sh.s_full0 + 8 * tile, s_phase, sh.abort_flag, 2 + tile, w, j)) return;
-            s_phase ^= 1u;
+            // single-tile items alternate S buffers (the second is tile 1's region)
+            const bool alt = single && ((j - item.kv0) & 1);
+            const uint32_t tSj = tS + (alt ? 128u : 0u);
+            if (alt) {
+                if (!wait_bar(sh.s_alt, sa_phase, sh.abort_flag, 2, w, j)) return;
+                sa_phase ^= 1u;
+            } else {
+                if (!wait_bar(sh.s_full0 + 8 * tile, s_phase, sh.abort_flag, 2 + tile, w, j)) return;
+                s_phase ^= 1u;
+            }
             ptx::tc_fence_after_sync();
             uint32_t s[128];
-            ptx::tmem_load_128cols(tS, s);
+            ptx::tmem_load_128cols(tSj, s);
             const int kvalid = key_lim - j * kBC;
             if constexpr ((MODE & kPaged) != 0) {
                 // bit s: box s lies in an unallocated page (warp-uniform)
@@ -750,11 +802,18 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
             // in its first tile); the guard keeps a fully masked row at p = 0.
             float se, sr;
             if constexpr (F8)
-                exp_pack_store128_e4m3(s, c2, m_ref == -INFINITY ? 0.f : kHeadroomF8 - m_ref, tS, se, sr);
+                exp_pack_store128_e4m3(s, c2, m_ref == -INFINITY ? 0.f : kHeadroomF8 - m_ref, tSj, se, sr);
             else
-                exp_pack_store128(s, c2, m_ref == -INFINITY ? 0.f : -m_ref, tS, se, sr);
+                exp_pack_store128(s, c2, m_ref == -INFINITY ? 0.f : -m_ref, tSj, se, sr);
             l += se;
             l_rounded += sr;
+            // single-tile items: S(j) ready no longer implies P(j-1) V done;
+            // wait for it before O may be rescaled (it is normally done by now)
+            if (single && j > item.kv0) {
+                if (!wait_bar(sh.pv_done, pv_phase, sh.abort_flag, 2, w, j)) return;
+                pv_phase ^= 1u;
+                ptx::tc_fence_after_sync();
+            }
             // Rescale O_t in TMEM when this warp's reference maximum moved
             // (PV_t(j-1) has completed, see the header; PV_t(j) waits for us).
             if (__any_sync(0xffffffffu, j > item.kv0 && alpha != 1.f)) {
@@ -836,9 +895,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     const uint32_t smem_q = base;
     const uint32_t smem_ring = base + C::kQBytes;
     const uint32_t bars = base + C::kBarOffset;
-    // barrier block: 9 fixed barriers, 2 * kSlots ring barriers, then the
+    // barrier block: 11 fixed barriers, 2 * kSlots ring barriers, then the
     // TMEM address holder and the abort flag
-    constexpr int kHolder = 72 + 16 * C::kSlots;
+    constexpr int kHolder = 88 + 16 * C::kSlots;
     static_assert(kHolder + 8 <= 256, "barrier block overflows its 256 bytes");
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(base_ptr + C::kBarOffset + kHolder);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base_ptr + C::kBarOffset + kHolder + 4);
@@ -850,8 +909,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     sh.p_full0 = bars + 32;       // 2
     sh.o_full0 = bars + 48;       // 2
     sh.done = bars + 64;
-    sh.kv_full0 = bars + 72;      // kSlots
-    sh.kv_empty0 = bars + 72 + 8 * C::kSlots;
+    sh.s_alt = bars + 72;
+    sh.pv_done = bars + 80;
+    sh.kv_full0 = bars + 88;      // kSlots
+    sh.kv_empty0 = bars + 88 + 8 * C::kSlots;
     sh.abort_flag = abort_flag;
 
     const int warp = threadIdx.x >> 5;
@@ -866,6 +927,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             ptx::mbar_init(sh.o_full0 + 8 * t, 1);
         }
         ptx::mbar_init(sh.done, 1);
+        ptx::mbar_init(sh.s_alt, 1);
+        ptx::mbar_init(sh.pv_done, 1);
         for (int s = 0; s < C::kSlots; ++s) {
             ptx::mbar_init(sh.kv_full0 + 8 * s, 1);
             ptx::mbar_init(sh.kv_empty0 + 8 * s, 1);
