@@ -89,6 +89,31 @@ def online_softmax_blocks(x, block):
     return m, l, steps
 
 
+def online_softmax_lagged(x, block, tau):
+    """The block recurrence with a lagging reference value (the reading of
+    "9.4 FlashAttention 与 FlashMLA" section 9.4.2 the GPU kernel uses): the
+    reference r is raised to a block's maximum only when that maximum exceeds
+    r by more than tau; otherwise the block is summed against the old r and the
+    rescale factor alpha is exactly 1.  The section's invariant
+    l^(k) = sum_{j <= k} exp(x_j - r^(k)) holds for any reference value, so the
+    result r + ln l equals the plain log-sum-exp; tau only bounds the terms,
+    exp(x - r) <= exp(tau).  Returns (r, l, [(r^(k), l^(k), alpha^(k)), ...])."""
+    x = np.asarray(x, dtype=np.float64)
+    r = -math.inf
+    l = 0.0
+    steps = []
+    for start in range(0, len(x), block):
+        xb = x[start:start + block]
+        m_block = float(np.max(xb))
+        alpha = 1.0
+        if m_block > r + tau:
+            alpha = math.exp(r - m_block)      # 0 on the first block
+            r = m_block
+        l = l * alpha + float(np.sum(np.exp(xb - r)))
+        steps.append((r, l, alpha))
+    return r, l, steps
+
+
 def blocked_attention(Q, K, V, scale, causal, Br, Bc):
     """Tiled attention forward for one head, fp64.
 

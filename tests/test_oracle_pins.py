@@ -366,3 +366,39 @@ def test_planted_mistake_is_caught(name, tmp_path):
         except (AssertionError, RuntimeError, ValueError, IndexError):
             caught += 1
     assert caught >= 1, f"no pin catches: {name}"
+
+
+@pytest.mark.parametrize("tau", [0.0, 8 * math.log(2.0), 20.0])
+@pytest.mark.parametrize("block", [1, 7, 128])
+def test_lagged_reference_softmax_equals_logsumexp(tau, block):
+    """The kernel's reading of the online softmax: the reference is raised only
+    when a block maximum exceeds it by more than tau (alpha is exactly 1
+    otherwise).  Any reference keeps l = sum exp(x - r), so r + ln l is the
+    log-sum-exp, and every term stays below exp(tau)."""
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(int(tau * 10) + block)
+    for x in (rng.standard_normal(1000) * 3, np.sort(rng.standard_normal(500) * 10),   # rising maxima
+              np.linspace(50, -50, 300), np.array([0.0])):
+        r, l, steps = online.online_softmax_lagged(x, block, tau)
+        assert abs((r + math.log(l)) - logsumexp(x)) < 1e-12 * max(1.0, abs(logsumexp(x)))
+        for k, (rk, lk, alpha) in enumerate(steps):   # the invariant at every block boundary
+            seen = x[:min(len(x), (k + 1) * block)]
+            assert abs(lk - np.sum(np.exp(seen - rk))) <= 1e-12 * lk
+            assert np.max(seen) - rk <= tau + 1e-12
+            if k > 0 and rk == steps[k - 1][0]:
+                assert alpha == 1.0
+
+
+def test_lagged_reference_with_a_dropped_rescale_is_caught():
+    # planted mistake: raising the reference without rescaling the old sum
+    x = np.sort(np.random.default_rng(9).standard_normal(400) * 8)
+    r, l, _ = online.online_softmax_lagged(x, 16, 2.0)
+    rr, ll = -math.inf, 0.0
+    for start in range(0, len(x), 16):
+        xb = x[start:start + 16]
+        if np.max(xb) > rr + 2.0:
+            rr = float(np.max(xb))                     # (alpha forgotten)
+        ll = ll + float(np.sum(np.exp(xb - rr)))
+    from scipy.special import logsumexp
+    assert abs(r + math.log(l) - logsumexp(x)) < 1e-12
+    assert abs(rr + math.log(ll) - logsumexp(x)) > 1e-3
