@@ -219,6 +219,37 @@ def fa_bwd(q, k, v, o, lse, do, dq=None, dk=None, dv=None, scale=None, causal=Fa
     return dq, dk, dv
 
 
+class _Attention(torch.autograd.Function):
+    """Autograd wrapper: forward through fa_fwd (saving O and LSE), backward
+    through fa_bwd.  Marshalling only; both directions run in the library."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, scale, causal):
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        o, lse = fa_fwd(q, k, v, scale=scale, causal=causal)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.scale, ctx.causal = scale, causal
+        ctx.mark_non_differentiable(lse)
+        return o, lse
+
+    @staticmethod
+    def backward(ctx, do, _dlse):
+        q, k, v, o, lse = ctx.saved_tensors
+        dq, dk, dv = fa_bwd(q, k, v, o, lse, do.contiguous(), scale=ctx.scale, causal=ctx.causal)
+        return dq, dk, dv, None, None
+
+
+def flash_attention(q, k, v, causal=False, scale=None, return_lse=False):
+    """softmax(scale * q k^T) v for bf16 CUDA tensors [B, H, N, d] (d = 64 or
+    128), differentiable with respect to q, k and v.  scale defaults to
+    1/sqrt(d); causal applies the top-left mask (key j visible to query i iff
+    j <= i).  Returns O, or (O, LSE) with return_lse."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    o, lse = _Attention.apply(q, k, v, float(scale), bool(causal))
+    return (o, lse) if return_lse else o
+
+
 def check_device_status(stream=None):
     """Synchronise and raise if a kernel of the library hit a wait limit."""
     _check(load_library().fa_check_device_status(_stream_handle(stream)))

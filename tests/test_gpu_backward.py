@@ -84,3 +84,22 @@ def test_backward_zero_upstream_gradient_gives_zero(ops):
     ops.check_device_status()
     for g in (dQ, dK, dV):
         assert torch.count_nonzero(g).item() == 0
+
+
+def test_autograd_wrapper_matches_the_oracle(ops):
+    # flash_attention(...).backward(dO) runs fa_fwd then fa_bwd; compare with the oracle
+    B, H, Nq, Nk, d = 1, 2, 200, 300, 64
+    q, k, v = inputs.custom_inputs(777, B, H, Nq, Nk, d)
+    do = inputs.normal_bf16(778, (B, H, Nq, d))
+    Q, K, V = (to_dev(a).requires_grad_(True) for a in (q, k, v))
+    O = ops.flash_attention(Q, K, V, causal=True)
+    O.backward(to_dev(do))
+    ops.check_device_status()
+    f = oracle.bf16_bits_to_f64
+    scale = 1 / math.sqrt(d)
+    O_ref, _ = oracle.attention(q, k, v, scale, True)
+    assert np.abs(O.detach().float().cpu().numpy() - O_ref).max() <= 2e-2
+    rQ, rK, rV = backward.backward_heads(f(q), f(k), f(v), f(do), scale, True)
+    check("dQ", Q.grad, rQ)
+    check("dK", K.grad, rK)
+    check("dV", V.grad, rV)
