@@ -519,11 +519,11 @@ extern "C" fa_status fa_fwd_host(const void *hQ, const void *hK, const void *hV,
 
 // ------------------------------------------------- split keys without allocating
 //
-// Some callers cannot allocate device memory where they call attention: code
-// being recorded into a CUDA graph (an allocation there is not replayed and
-// cudaMalloc may synchronise the device), serving loops with a latency budget
-// that rules out the allocator, frameworks whose allocator owns all memory up
-// front, and plugins handed only the tensors they read and write.  For them the
+// Some callers cannot allocate device memory where they call attention: serving
+// loops with a latency budget that rules out the allocator (cudaMalloc may
+// synchronise the device), frameworks whose allocator owns all memory up front,
+// and plugins that an inference runtime hands only the tensors they read and
+// write and forbids to allocate while they execute.  For them the
 // split-key forward can put its partial results in a scratch area that lives in
 // this file: a fixed array in device global memory, which every GPU that loads
 // the library holds until the process exits.  Its host-side name is only a

@@ -265,10 +265,10 @@ fa_status fa_bwd_workspace(int B, int H, int Nq, int Nk, int d, size_t *bytes);
 
 /*
  * fa_fwd_splitkv_noalloc -- fa_fwd_splitkv for callers that cannot allocate
- * device memory: code being recorded into a CUDA graph (an allocation is not
- * replayed, and cudaMalloc may synchronise the device), serving loops whose
- * latency budget rules out the allocator, frameworks whose allocator owns all
- * memory up front, plugins handed only their input and output tensors.  The
+ * device memory: serving loops whose latency budget rules out the allocator
+ * (cudaMalloc may synchronise the device), frameworks whose allocator owns all
+ * memory up front, plugins that an inference runtime hands only their input
+ * and output tensors and forbids to allocate while they execute.  The
  * pages have no counterpart; this is a property of the library, not of the
  * method.
  *

@@ -1,9 +1,10 @@
 """The no-allocation split-key entry point, fa_fwd_splitkv_noalloc.
 
 Some callers cannot allocate device memory at the moment they run attention:
-code being recorded into a CUDA graph, serving loops whose latency budget rules
-out the allocator, frameworks whose allocator owns all memory up front, or
-plugins handed only the tensors they read and write.  This entry point serves
+serving loops whose latency budget rules out the allocator (cudaMalloc may
+synchronise the device), frameworks whose allocator owns all memory up front,
+or plugins that an inference runtime hands only the tensors they read and
+write and forbids to allocate while they execute.  This entry point serves
 them: its partial results live in a fixed 16 MiB scratch array inside the
 library rather than in a workspace the caller allocates.
 
