@@ -1,5 +1,6 @@
 // Host side of libfa_gb300.so: argument validation, TMA tensor maps, the
 // persistent schedule, and the launch.  Implements the C ABI of include/fa.h.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -496,6 +497,71 @@ extern "C" fa_status fa_schedule(int B, int H, int Nq, int Nk, int d, int causal
     return n == p.n_items ? FA_OK : FA_ERR_INVALID_ARG;
 }
 
+// ------------------------------------------------------------ host buffers
+//
+// fa_fwd_host moves the inputs in and the outputs out around the forward.  A
+// large call is cut into up to kHostChunksMax groups of heads that flow
+// through three internal streams: while group c is being computed, group c+1
+// is copied in and group c-1 is copied out, so the two copy directions and
+// the tensor cores work at the same time.  The streams and events are created
+// once per device and shared by all calls (enqueueing is serialised).
+
+namespace {
+
+constexpr int kHostChunksMax = 8;
+constexpr size_t kHostChunkMinBytes = size_t{8} << 20;   // input bytes per group, at least
+
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t h2d[2] = {nullptr, nullptr}, comp = nullptr, d2h = nullptr;
+    cudaEvent_t start = nullptr, end = nullptr;
+    cudaEvent_t in_done[kHostChunksMax] = {}, out_ready[kHostChunksMax] = {};
+};
+HostPipe g_pipe[64];
+std::mutex g_pipe_mu;   // held while a call enqueues (the streams and events are shared)
+
+// The current device's streams and events (created on first use).  Caller
+// holds g_pipe_mu.
+fa_status host_pipe(HostPipe *&out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FA_ERR_CUDA;
+    HostPipe &hp = g_pipe[dev];
+    if (!hp.ready) {
+        bool ok = true;
+        for (cudaStream_t *st : {&hp.h2d[0], &hp.h2d[1], &hp.comp, &hp.d2h})
+            ok = ok && cudaStreamCreateWithFlags(st, cudaStreamNonBlocking) == cudaSuccess;
+        ok = ok && cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&hp.end, cudaEventDisableTiming) == cudaSuccess;
+        for (int c = 0; c < kHostChunksMax && ok; ++c)
+            ok = cudaEventCreateWithFlags(&hp.in_done[c], cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&hp.out_ready[c], cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) return FA_ERR_CUDA;
+        hp.ready = true;
+    }
+    out = &hp;
+    return FA_OK;
+}
+
+// Number of head groups for a call: enough input bytes per group that each
+// copy runs at full speed, and about a full wave of work items per group so
+// that splitting costs the kernel little.
+int host_chunks(int64_t BH, int Nq, int Nk, int d, int sms) {
+    const size_t in_bytes = static_cast<size_t>(BH) * (static_cast<size_t>(Nq) + 2 * static_cast<size_t>(Nk)) * d * 2;
+    const int64_t items = BH * ((((Nq + fa::kBR - 1) / fa::kBR) + 1) / 2);
+    int64_t c = static_cast<int64_t>(in_bytes / kHostChunkMinBytes);
+    c = std::min<int64_t>(c, items / std::max(sms, 1));
+    c = std::min<int64_t>(c, kHostChunksMax);
+    c = std::min<int64_t>(c, BH);
+    return static_cast<int>(std::max<int64_t>(c, 1));
+}
+
+}  // namespace
+
+extern "C" int fa_host_groups(int B, int H, int Nq, int Nk, int d, int num_sms) {
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || (d != 64 && d != 128) || num_sms < 1) return 0;
+    return host_chunks(static_cast<int64_t>(B) * H, Nq, Nk, d, num_sms);
+}
+
 extern "C" fa_status fa_fwd_host(const void *hQ, const void *hK, const void *hV, void *hO, float *hLSE,
                                  void *dQ, void *dK, void *dV, void *dO, float *dLSE, int B, int H, int Nq,
                                  int Nk, int d, float scale, int causal, fa_stream_t stream) {
@@ -503,16 +569,64 @@ extern "C" fa_status fa_fwd_host(const void *hQ, const void *hK, const void *hV,
     fa_status st = validate(dQ, dK, dV, dO, dLSE, B, H, Nq, Nk, d, scale);
     if (st != FA_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const size_t BH = static_cast<size_t>(B) * H;
-    const size_t q_bytes = BH * Nq * d * 2, kv_bytes = BH * Nk * d * 2, lse_bytes = BH * Nq * 4;
-    if (cudaMemcpyAsync(dQ, hQ, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(dK, hK, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(dV, hV, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return FA_ERR_CUDA;
-    st = fa_fwd(dQ, dK, dV, dO, dLSE, B, H, Nq, Nk, d, scale, causal, stream);
+    const int64_t BH = static_cast<int64_t>(B) * H;
+    const size_t q_head = static_cast<size_t>(Nq) * d * 2, kv_head = static_cast<size_t>(Nk) * d * 2;
+    const size_t lse_head = static_cast<size_t>(Nq) * 4;
+    int sms;
+    DeviceInfo *info;
+    st = device_info(sms, info);
     if (st != FA_OK) return st;
-    if (cudaMemcpyAsync(hO, dO, q_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        cudaMemcpyAsync(hLSE, dLSE, lse_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    const int chunks = host_chunks(BH, Nq, Nk, d, sms);
+    auto cp = [](void *dst, const void *src, size_t n, cudaMemcpyKind k, cudaStream_t on) {
+        return cudaMemcpyAsync(dst, src, n, k, on) == cudaSuccess;
+    };
+    auto at = [](const void *base, size_t off) { return static_cast<const char *>(base) + off; };
+    auto at_mut = [](void *base, size_t off) { return static_cast<char *>(base) + off; };
+    if (chunks == 1) {
+        if (!cp(dQ, hQ, BH * q_head, cudaMemcpyHostToDevice, s) || !cp(dK, hK, BH * kv_head, cudaMemcpyHostToDevice, s) ||
+            !cp(dV, hV, BH * kv_head, cudaMemcpyHostToDevice, s))
+            return FA_ERR_CUDA;
+        st = fa_fwd(dQ, dK, dV, dO, dLSE, B, H, Nq, Nk, d, scale, causal, stream);
+        if (st != FA_OK) return st;
+        if (!cp(hO, dO, BH * q_head, cudaMemcpyDeviceToHost, s) || !cp(hLSE, dLSE, BH * lse_head, cudaMemcpyDeviceToHost, s))
+            return FA_ERR_CUDA;
+        return FA_OK;
+    }
+
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    HostPipe *hp;
+    st = host_pipe(hp);
+    if (st != FA_OK) return st;
+    // fork: the internal streams start after the caller's earlier work on `s`
+    if (cudaEventRecord(hp->start, s) != cudaSuccess) return FA_ERR_CUDA;
+    for (cudaStream_t x : {hp->h2d[0], hp->h2d[1], hp->comp, hp->d2h})
+        if (cudaStreamWaitEvent(x, hp->start, 0) != cudaSuccess) return FA_ERR_CUDA;
+    bool ok = true;
+    for (int c = 0; c < chunks && ok; ++c) {
+        const int64_t h0 = BH * c / chunks, h1 = BH * (c + 1) / chunks;
+        const size_t n = static_cast<size_t>(h1 - h0);
+        cudaStream_t in = hp->h2d[c & 1];
+        ok = cp(at_mut(dQ, h0 * q_head), at(hQ, h0 * q_head), n * q_head, cudaMemcpyHostToDevice, in) &&
+             cp(at_mut(dK, h0 * kv_head), at(hK, h0 * kv_head), n * kv_head, cudaMemcpyHostToDevice, in) &&
+             cp(at_mut(dV, h0 * kv_head), at(hV, h0 * kv_head), n * kv_head, cudaMemcpyHostToDevice, in) &&
+             cudaEventRecord(hp->in_done[c], in) == cudaSuccess &&
+             cudaStreamWaitEvent(hp->comp, hp->in_done[c], 0) == cudaSuccess;
+        if (ok)   // the group's heads are a contiguous [1, n, N, d] block of each tensor
+            ok = run_forward(at(dQ, h0 * q_head), at(dK, h0 * kv_head), at(dV, h0 * kv_head), at_mut(dO, h0 * q_head),
+                             reinterpret_cast<float *>(at_mut(dLSE, h0 * lse_head)), 1, static_cast<int>(n), Nq, Nk,
+                             d, scale, causal, 1, nullptr, nullptr, hp->comp) == FA_OK;
+        ok = ok && cudaEventRecord(hp->out_ready[c], hp->comp) == cudaSuccess &&
+             cudaStreamWaitEvent(hp->d2h, hp->out_ready[c], 0) == cudaSuccess &&
+             cp(at_mut(hO, h0 * q_head), at(dO, h0 * q_head), n * q_head, cudaMemcpyDeviceToHost, hp->d2h) &&
+             cp(at_mut(hLSE, h0 * lse_head), at(dLSE, h0 * lse_head), n * lse_head, cudaMemcpyDeviceToHost, hp->d2h);
+    }
+    if (!ok) {
+        // leave nothing of this call running unordered with the caller's stream
+        for (cudaStream_t x : {hp->h2d[0], hp->h2d[1], hp->comp, hp->d2h}) cudaStreamSynchronize(x);
+        return FA_ERR_CUDA;
+    }
+    // join: the last copy out follows every compute, and each compute its copies in
+    if (cudaEventRecord(hp->end, hp->d2h) != cudaSuccess || cudaStreamWaitEvent(s, hp->end, 0) != cudaSuccess)
         return FA_ERR_CUDA;
     return FA_OK;
 }

@@ -40,6 +40,8 @@ def load_library(path: str | None = None):
     lib.fa_fwd.restype = i
     lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
     lib.fa_fwd_host.restype = i
+    lib.fa_host_groups.argtypes = [i, i, i, i, i, i]
+    lib.fa_host_groups.restype = i
     lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, ctypes.c_size_t, vp]
     lib.fa_fwd_splitkv.restype = i
     lib.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
@@ -121,6 +123,11 @@ def fa_fwd_host(hq, hk, hv, ho, hlse, dq, dk, dv, do, dlse, scale, causal=False,
                                       hlse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                                       do.data_ptr(), dlse.data_ptr(), B, H, Nq, Nk, d, scale,
                                       int(bool(causal)), _stream_handle(stream)))
+
+
+def host_groups(B, H, Nq, Nk, d, num_sms):
+    """Number of head groups fa_fwd_host pipelines for these shapes (1: none)."""
+    return int(load_library().fa_host_groups(B, H, Nq, Nk, d, num_sms))
 
 
 def fa_fwd_paged(q, k_cache, v_cache, block_table, seq_lens, o=None, lse=None, scale=None, causal=False,

@@ -74,16 +74,33 @@ fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LS
 
 /*
  * fa_fwd_host -- the same operation end to end from host memory: copies hQ,
- * hK, hV to the caller's device buffers dQ, dK, dV, runs fa_fwd, and copies
- * dO, dLSE back to hO, hLSE, all enqueued on `stream` in that order.  Host
- * buffers should be pinned (page-locked) for the copies to be asynchronous.
- * Shapes, layouts, alignment and errors are those of fa_fwd; the call does
- * not wait for completion (synchronise the stream before reading hO, hLSE).
+ * hK, hV to the caller's device buffers dQ, dK, dV, runs the forward, and
+ * copies dO, dLSE back to hO, hLSE.  Host buffers should be pinned
+ * (page-locked) for the copies to be asynchronous.  Shapes, layouts,
+ * alignment and errors are those of fa_fwd; the call does not wait for
+ * completion (synchronise `stream` before reading hO, hLSE).
+ *
+ * A large call is split into groups of whole heads (fa_host_groups says how
+ * many) that are pipelined: group c is computed while group c+1 is copied in
+ * and group c-1 copied out, on streams internal to the library that fork
+ * from `stream` (after the work already enqueued on it) and join back into it
+ * (later work on `stream` sees every output).  The result is bit-identical to
+ * fa_fwd on the same device buffers.  The internal streams are created on the
+ * first pipelined call on a device and kept until the process exits.
  */
 fa_status fa_fwd_host(const void *hQ, const void *hK, const void *hV, void *hO, float *hLSE,
                       void *dQ, void *dK, void *dV, void *dO, float *dLSE,
                       int B, int H, int Nq, int Nk, int d, float scale, int causal,
                       fa_stream_t stream);
+
+/*
+ * fa_host_groups -- how many head groups fa_fwd_host pipelines for these
+ * shapes on a GPU with num_sms SMs (host only; no GPU needed): at least
+ * 8 MiB of inputs and about one full wave of work items per group, at most 8
+ * groups and one head per group.  1 means no pipelining.  Returns 0 for
+ * invalid sizes.
+ */
+int fa_host_groups(int B, int H, int Nq, int Nk, int d, int num_sms);
 
 /*
  * fa_check_device_status -- synchronises `stream`, then reads and clears the

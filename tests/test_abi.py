@@ -186,3 +186,16 @@ def test_quantize_argument_errors(lib, kw, expected):
     st = lib.fa_quantize_fp8(a["x"], a["x8"], a["descale"], a["B"], a["H"], a["N"], a["d"], a["signs"] or None,
                              a["transpose"], None)
     assert st == expected
+
+
+def test_host_groups_rule(lib):
+    # small calls are not pipelined; a group keeps >= 8 MiB of inputs and about
+    # a wave of work items; at most 8 groups and one head per group
+    assert ops.host_groups(1, 1, 256, 256, 64, 152) == 1
+    assert ops.host_groups(2, 16, 4096, 4096, 128, 152) == 3     # 512 items / 152 SMs
+    assert ops.host_groups(3, 17, 2048, 2048, 128, 152) == 2
+    assert ops.host_groups(1, 32, 16384, 16384, 128, 152) == 8   # capped at 8
+    assert ops.host_groups(1, 2, 65536, 65536, 128, 1) == 2      # capped at one head per group
+    assert ops.host_groups(8, 32, 128, 8192, 128, 152) == 1      # one query tile per head: 256 items
+    for bad in [(0, 1, 1, 1, 64, 1), (1, 1, 1, 1, 96, 1), (1, 1, 1, 1, 64, 0)]:
+        assert ops.host_groups(*bad) == 0

@@ -236,6 +236,36 @@ def test_host_buffer_entry_point(ops):
     assert_close(ho, hl, O_ref, L_ref, "host entry")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_host_buffer_entry_point_pipelined_groups(ops, causal):
+    # 51 heads of 2048 rows: fa_fwd_host pipelines them in ragged groups of
+    # heads; each group runs the same kernel on its heads, so the result is
+    # bit-identical to one fa_fwd over the device buffers.
+    B, H, Nq, Nk, d = 3, 17, 2048, 2048, 128
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    groups = ops.host_groups(B, H, Nq, Nk, d, sms)
+    assert groups >= 2
+    scale = float(np.float32(1 / math.sqrt(d)))
+    q, k, v = inputs.custom_inputs(77, B, H, Nq, Nk, d)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
+    hq, hk, hv = pin(q), pin(k), pin(v)
+    ho = torch.full((B, H, Nq, d), float("nan"), dtype=torch.bfloat16).pin_memory()
+    hl = torch.full((B, H, Nq), float("nan"), dtype=torch.float32).pin_memory()
+    dq, dk, dv = (torch.empty_like(t, device="cuda") for t in (hq, hk, hv))
+    do = torch.empty_like(ho, device="cuda")
+    dl = torch.empty_like(hl, device="cuda")
+    stream = torch.cuda.Stream()
+    ops.fa_fwd_host(hq, hk, hv, ho, hl, dq, dk, dv, do, dl, scale, causal=causal, stream=stream)
+    stream.synchronize()
+    ops.check_device_status()
+    o_ref, l_ref = run_gpu(ops, q, k, v, scale, causal)
+    assert torch.equal(ho, o_ref.cpu()) and torch.equal(hl, l_ref.cpu())
+    rows = sample_rows(B, H, Nq, n_random=256, seed=5)
+    Or, Lr = oracle.attention_rows(q, k, v, scale, causal, rows=rows)
+    sel = torch.from_numpy(rows)
+    assert_close(ho.reshape(-1, d)[sel], hl.reshape(-1)[sel], Or, Lr, "pipelined host entry")
+
+
 # ------------------------------------------------------------- split keys
 
 def run_split(ops, q, k, v, scale, causal, splits):
