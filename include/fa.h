@@ -96,9 +96,9 @@ fa_status fa_fwd_host(const void *hQ, const void *hK, const void *hV, void *hO, 
 /*
  * fa_host_groups -- how many head groups fa_fwd_host pipelines for these
  * shapes on a GPU with num_sms SMs (host only; no GPU needed): at least
- * 8 MiB of inputs and about one full wave of work items per group, at most 8
- * groups and one head per group.  1 means no pipelining.  Returns 0 for
- * invalid sizes.
+ * 8 MiB of inputs per group, at most 8 groups and one head per group (the
+ * SM count does not change the answer at present).  1 means no pipelining.
+ * Returns 0 for invalid sizes.
  */
 int fa_host_groups(int B, int H, int Nq, int Nk, int d, int num_sms);
 

@@ -189,13 +189,15 @@ def test_quantize_argument_errors(lib, kw, expected):
 
 
 def test_host_groups_rule(lib):
-    # small calls are not pipelined; a group keeps >= 8 MiB of inputs and about
-    # a wave of work items; at most 8 groups and one head per group
+    # small calls are not pipelined; a group keeps >= 8 MiB of inputs; at most
+    # 8 groups and one head per group
     assert ops.host_groups(1, 1, 256, 256, 64, 152) == 1
-    assert ops.host_groups(2, 16, 4096, 4096, 128, 152) == 3     # 512 items / 152 SMs
-    assert ops.host_groups(3, 17, 2048, 2048, 128, 152) == 2
-    assert ops.host_groups(1, 32, 16384, 16384, 128, 152) == 8   # capped at 8
+    assert ops.host_groups(1, 4, 1024, 1024, 128, 152) == 1      # 3 MiB of inputs
+    assert ops.host_groups(1, 16, 1024, 1024, 128, 152) == 1     # 12 MiB: one group of 8 MiB
+    assert ops.host_groups(1, 16, 1024, 2048, 128, 152) == 2     # 20 MiB
+    assert ops.host_groups(2, 16, 4096, 4096, 128, 152) == 8     # 96 MiB, capped at 8
+    assert ops.host_groups(3, 17, 2048, 2048, 128, 152) == 8
     assert ops.host_groups(1, 2, 65536, 65536, 128, 1) == 2      # capped at one head per group
-    assert ops.host_groups(8, 32, 128, 8192, 128, 152) == 1      # one query tile per head: 256 items
+    assert ops.host_groups(8, 32, 128, 8192, 128, 152) == 8
     for bad in [(0, 1, 1, 1, 64, 1), (1, 1, 1, 1, 96, 1), (1, 1, 1, 1, 64, 0)]:
         assert ops.host_groups(*bad) == 0
