@@ -64,13 +64,7 @@ constexpr uint32_t kSoftmaxRegs = 208;  // after setmaxnreg; launch gives 168
 constexpr uint32_t kOtherRegs = 88;     // producer / MMA warpgroup
 static_assert(kSoftmaxRegs * 256 + kOtherRegs * 128 <= 168 * kThreads, "register split exceeds the launch allocation");
 constexpr int kChunkBytes = 128 * 128;  // one [128 rows x 64 bf16] swizzled TMA box
-// bf16 P: the reference maximum sits kHeadroom (log2 units) above the first
-// visible tile's row maximum, so weights are <= 2^-32 there; it is raised only
-// when a tile's weights sum past kSumBound (a key 89 log2 units above that
-// maximum).  Keys more than 94 log2 units below it flush to zero (relative
-// weight < 2^-94).
-constexpr float kHeadroom = 32.0f;
-constexpr float kSumBound = 18446744073709551616.0f;   // 2^64
+constexpr float kTau = 8.0f;            // log2-domain slack before the max is raised
 // E4M3 P: a smaller slack and a headroom, p = 2^(c*s - m + 4) in (0, 2^8]:
 // the row maximum's weight lands in [2^4, 2^8] (E4M3 reaches 448), so keys
 // up to 14 log2 units below it stay above E4M3's smallest subnormal 2^-9
@@ -794,43 +788,25 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
                         if (c >= kvalid) s[c] = __float_as_uint(mask_val);
                 }
             }
-            // m_ref is finite once a row has seen a key (every row sees key 0
-            // in its first tile); the guards keep a fully masked row at p = 0.
+            const float mx = row_extreme128(s, pos);
+            const float m_tile = kvalid > 0 ? mx * c2 : -INFINITY;
             float alpha = 1.f;
-            float se, sr;
-            if constexpr (F8) {
-                // E4M3 P: the reference follows the row maximum within kTauF8
-                const float mx = row_extreme128(s, pos);
-                const float m_tile = kvalid > 0 ? mx * c2 : -INFINITY;
-                if (m_tile > m_ref + kTauF8) {
-                    alpha = ptx::ex2(m_ref - m_tile);   // 0 on the first visible tile
-                    m_ref = m_tile;
-                }
-                exp_pack_store128_e4m3(s, c2, m_ref == -INFINITY ? 0.f : kHeadroomF8 - m_ref, tSj, se, sr);
-            } else {
-                // bf16 P: the reference is set once, kHeadroom above the first
-                // visible tile's maximum, and raised only when a tile's weights
-                // sum past kSumBound; the common step computes no maximum.
-                if (__any_sync(0xffffffffu, m_ref == -INFINITY)) {   // warp-uniform
-                    const float mx = row_extreme128(s, pos);
-                    const float m_tile = kvalid > 0 ? mx * c2 : -INFINITY;
-                    // l = 0 and O holds no weight of this row yet: nothing to rescale
-                    if (m_ref == -INFINITY && m_tile != -INFINITY) m_ref = m_tile + kHeadroom;
-                }
-                exp_pack_store128(s, c2, m_ref == -INFINITY ? 0.f : -m_ref, tSj, se, sr);
-                if (__any_sync(0xffffffffu, !(se <= kSumBound))) {   // warp-uniform, rare
-                    if (!(se <= kSumBound)) {
-                        // a weight above 2^57: raise the reference to this
-                        // tile's maximum + kHeadroom and redo the tile's P
-                        const float m_new = row_extreme128(s, pos) * c2 + kHeadroom;
-                        alpha = ptx::ex2(m_ref - m_new);
-                        m_ref = m_new;
-                        exp_pack_store128(s, c2, -m_ref, tSj, se, sr);
-                    }
-                }
+            if (m_tile > m_ref + (F8 ? kTauF8 : kTau)) {
+                alpha = ptx::ex2(m_ref - m_tile);   // 0 on the first visible tile
+                m_ref = m_tile;
             }
-            l = l * alpha + se;
-            l_rounded = l_rounded * alpha + sr;
+            l *= alpha;
+            l_rounded *= alpha;
+
+            // m_ref is finite once a row has seen a key (every row sees key 0
+            // in its first tile); the guard keeps a fully masked row at p = 0.
+            float se, sr;
+            if constexpr (F8)
+                exp_pack_store128_e4m3(s, c2, m_ref == -INFINITY ? 0.f : kHeadroomF8 - m_ref, tSj, se, sr);
+            else
+                exp_pack_store128(s, c2, m_ref == -INFINITY ? 0.f : -m_ref, tSj, se, sr);
+            l += se;
+            l_rounded += sr;
             // single-tile items: S(j) ready no longer implies P(j-1) V done;
             // wait for it before O may be rescaled (it is normally done by now)
             if (single && j > item.kv0) {

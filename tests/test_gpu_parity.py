@@ -266,6 +266,48 @@ def test_host_buffer_entry_point_pipelined_groups(ops, causal):
     assert_close(ho.reshape(-1, d)[sel], hl.reshape(-1)[sel], Or, Lr, "pipelined host entry")
 
 
+def test_host_entry_point_orders_after_earlier_work_and_serves_two_threads(ops):
+    # The pipelined path forks from the caller's stream after the work already
+    # on it: here the host inputs are only written by a copy enqueued just
+    # before the call.  Two host threads calling at once on their own streams
+    # both get their own, correct results.
+    import threading
+    B, H, Nq, Nk, d = 2, 16, 1024, 1024, 128
+    assert ops.host_groups(B, H, Nq, Nk, d, 152) >= 2
+    scale = float(np.float32(1 / math.sqrt(d)))
+
+    def one_call(seed, results, slot):
+        q, k, v = inputs.custom_inputs(seed, B, H, Nq, Nk, d)
+        src = [to_dev(a) for a in (q, k, v)]
+        host = [torch.zeros(t.shape, dtype=torch.bfloat16).pin_memory() for t in src]
+        ho = torch.empty((B, H, Nq, d), dtype=torch.bfloat16).pin_memory()
+        hl = torch.empty((B, H, Nq), dtype=torch.float32).pin_memory()
+        dev = [torch.empty_like(t) for t in src]
+        do = torch.empty_like(dev[0])
+        dl = torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")
+        stream = torch.cuda.Stream()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for h, t in zip(host, src):
+                h.copy_(t, non_blocking=True)       # the inputs reach host memory on `stream` only
+        ops.fa_fwd_host(*host, ho, hl, *dev, do, dl, scale, causal=True, stream=stream)
+        stream.synchronize()
+        o_ref, l_ref = ops.fa_fwd(*src, scale=scale, causal=True)
+        torch.cuda.synchronize()
+        results[slot] = torch.equal(ho, o_ref.cpu()) and torch.equal(hl, l_ref.cpu())
+
+    results = [None, None]
+    one_call(301, results, 0)
+    assert results[0]
+    threads = [threading.Thread(target=one_call, args=(400 + i, results, i)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    ops.check_device_status()
+    assert results == [True, True]
+
+
 # ------------------------------------------------------------- split keys
 
 def run_split(ops, q, k, v, scale, causal, splits):
