@@ -160,6 +160,7 @@ int setup_params(fa::FwdParams &p, int B, int H, int Nq, int Nk, int d, float sc
     p.c2 = static_cast<float>(c2);
     p.heads_per_group = heads_per_group(BH, Nk, d, causal);
     p.kv_splits = kv_splits > 1 ? kv_splits : 1;
+    p.drop_load_item = -1;
     if (p.kv_splits > 1) {
         const int64_t NP = static_cast<int64_t>(p.BH) * p.P;
         p.n_pair_items = static_cast<int>(NP);
@@ -244,7 +245,7 @@ fa_status device_info(int &sms, DeviceInfo *&out) {
 // kv_splits > 1, into O_part / LSE_part).
 fa_status run_forward(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int Nq,
                       int Nk, int d, float scale, int causal, int kv_splits, float *O_part, float *LSE_part,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, int drop_load_item = -1) {
     int sms;
     DeviceInfo *info;
     fa_status st = device_info(sms, info);
@@ -258,6 +259,7 @@ fa_status run_forward(const void *Q, const void *K, const void *V, void *O, floa
     p.LSE = LSE;
     p.O_part = O_part;
     p.LSE_part = LSE_part;
+    p.drop_load_item = drop_load_item;
     std::lock_guard<std::mutex> lock(g_dev_mu);
     return kv_splits > 1 ? launch_mode<fa::kSplit>(p, d, grid, stream, info->attr)
                          : launch_mode<fa::kDense>(p, d, grid, stream, info->attr);
@@ -283,6 +285,18 @@ extern "C" fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O
     if (st != FA_OK) return st;
     return run_forward(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, causal, 1, nullptr, nullptr,
                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+// The forward with one K tile deliberately left unloaded: exercises the
+// bounded waits and the clean shutdown of the kernel (see the header).
+extern "C" fa_status fa_fwd_test_missing_load(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
+                                              int H, int Nq, int Nk, int d, float scale, int causal, int item,
+                                              fa_stream_t stream) {
+    fa_status st = validate(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale);
+    if (st != FA_OK) return st;
+    if (item < 0) return FA_ERR_INVALID_ARG;
+    return run_forward(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, causal, 1, nullptr, nullptr,
+                       reinterpret_cast<cudaStream_t>(stream), item);
 }
 
 namespace {

@@ -139,6 +139,9 @@ struct FwdParams {
     const float *descale_q, *descale_k, *descale_v;
     int causal;
     float c2;          // scale * log2(e)
+    // test hook (fa_fwd_test_missing_load): the first K tile of this work
+    // item is never loaded, so a bounded wait expires; -1 in every other call
+    int drop_load_item;
 };
 
 struct Item {
@@ -388,6 +391,7 @@ __device__ void producer_role(const FwdParams &p, const Shared &sh, uint32_t sme
                     break;
                 }
                 const uint32_t full = sh.kv_full0 + 8 * slot;
+                if (w == p.drop_load_item && j == item.kv0 && which == 0) continue;   // test hook
                 ptx::mbar_arrive_expect_tx(full, C::kKVTileBytes);
                 const CUtensorMap *map = which ? &p.tmV : &p.tmK;
                 if constexpr ((MODE & kPaged) != 0) {

@@ -42,6 +42,8 @@ def load_library(path: str | None = None):
     lib.fa_fwd_host.restype = i
     lib.fa_host_groups.argtypes = [i, i, i, i, i, i]
     lib.fa_host_groups.restype = i
+    lib.fa_fwd_test_missing_load.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
+    lib.fa_fwd_test_missing_load.restype = i
     lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, ctypes.c_size_t, vp]
     lib.fa_fwd_splitkv.restype = i
     lib.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
@@ -123,6 +125,20 @@ def fa_fwd_host(hq, hk, hv, ho, hlse, dq, dk, dv, do, dlse, scale, causal=False,
                                       hlse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                                       do.data_ptr(), dlse.data_ptr(), B, H, Nq, Nk, d, scale,
                                       int(bool(causal)), _stream_handle(stream)))
+
+
+def fa_fwd_test_missing_load(q, k, v, item=0, scale=None, causal=False, stream=None):
+    """fa_fwd with the first K tile of work item `item` never loaded (tests the
+    bounded waits); returns the launch status, and the device status word then
+    reads FA_ERR_TIMEOUT."""
+    B, H, Nq, Nk, d = _shape(q, k)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    return int(load_library().fa_fwd_test_missing_load(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                                        lse.data_ptr(), B, H, Nq, Nk, d, scale, int(bool(causal)),
+                                                        item, _stream_handle(stream)))
 
 
 def host_groups(B, H, Nq, Nk, d, num_sms):

@@ -103,6 +103,21 @@ fa_status fa_fwd_host(const void *hQ, const void *hK, const void *hV, void *hO, 
 int fa_host_groups(int B, int H, int Nq, int Nk, int d, int num_sms);
 
 /*
+ * fa_fwd_test_missing_load -- fa_fwd with one deliberate failure, for testing
+ * the library's failure detection: the first K tile of work item `item` (an
+ * index into the list fa_schedule returns, 0 is always valid) is never
+ * loaded.  The kernel's wait for it gives up after its one-second limit, the
+ * kernel stops every role, waits (again with a limit) for the copies and
+ * MMAs it started, releases its tensor memory and exits; the GPU context
+ * stays usable.  fa_check_device_status then returns FA_ERR_TIMEOUT and O,
+ * LSE are undefined.  The pages have no counterpart; this is a property of
+ * the library.  Arguments as fa_fwd; item < 0 gives FA_ERR_INVALID_ARG.
+ */
+fa_status fa_fwd_test_missing_load(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                                   int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                                   int item, fa_stream_t stream);
+
+/*
  * fa_check_device_status -- synchronises `stream`, then reads and clears the
  * device status word that kernels of this library set when one of their
  * bounded waits expires.  Returns FA_OK, FA_ERR_TIMEOUT, or FA_ERR_CUDA if the
