@@ -237,11 +237,12 @@ def test_host_buffer_entry_point(ops):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-def test_host_buffer_entry_point_pipelined_groups(ops, causal):
-    # 51 heads of 2048 rows: fa_fwd_host pipelines them in ragged groups of
-    # heads (8 groups of 6 or 7); each group runs the same kernel on its heads, so the result is
-    # bit-identical to one fa_fwd over the device buffers.
-    B, H, Nq, Nk, d = 3, 17, 2048, 2048, 128
+@pytest.mark.parametrize("d,N", [(128, 2048), (64, 4096)])
+def test_host_buffer_entry_point_pipelined_groups(ops, causal, d, N):
+    # 51 heads: fa_fwd_host pipelines them in ragged groups of heads (8 groups
+    # of 6 or 7); each group runs the same kernel on its heads, so the result
+    # is bit-identical to one fa_fwd over the device buffers.
+    B, H, Nq, Nk = 3, 17, N, N
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     groups = ops.host_groups(B, H, Nq, Nk, d, sms)
     assert groups >= 2
