@@ -37,16 +37,16 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [BH][N][d] bf16, boxes of 64 columns x 128 rows x 1 head, 128-byte swizzle.
-// Rows past N inside a head read as zero (the map is 3-D, so a box never
-// spills into the next head).
-bool make_map(CUtensorMap *map, const void *ptr, int64_t BH, int64_t N, int d) {
+// [BH][N][d] bf16, boxes of 64 columns x box_rows rows x 1 head, 128-byte
+// swizzle.  Rows past N inside a head read as zero (the map is 3-D, so a box
+// never spills into the next head).
+bool make_map(CUtensorMap *map, const void *ptr, int64_t BH, int64_t N, int d, int box_rows = fa::kBR) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                                 static_cast<cuuint64_t>(BH)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
-    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(fa::kBR), 1};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -54,7 +54,8 @@ bool make_map(CUtensorMap *map, const void *ptr, int64_t BH, int64_t N, int d) {
 }
 
 // Paged cache [num_blocks][H][block_size][d] bf16, boxes of 64 columns x
-// min(block_size, 128) rows of one head of one block, 128-byte swizzle.
+// min(block_size, keys per K/V tile) rows of one head of one block, 128-byte
+// swizzle.
 bool make_map_paged(CUtensorMap *map, const void *ptr, int num_blocks, int H, int block_size, int d) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
@@ -62,7 +63,8 @@ bool make_map_paged(CUtensorMap *map, const void *ptr, int num_blocks, int H, in
                                 static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(num_blocks)};
     const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(block_size) * d * 2,
                                    static_cast<cuuint64_t>(H) * block_size * d * 2};
-    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(block_size < fa::kBC ? block_size : fa::kBC), 1, 1};
+    const int bc = fa::kv_tile_keys(d);
+    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(block_size < bc ? block_size : bc), 1, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -138,9 +140,13 @@ int heads_per_group(int64_t BH, int64_t Nk, int d, int causal) {
     return static_cast<int>(hg);
 }
 
+// Persistent CTAs per SM of the forward for head dimension d.
+int ctas_per_sm(int d) { return d == 64 ? fa::Config<64>::kCtasPerSm : fa::Config<128>::kCtasPerSm; }
+
 // Shapes, scale and schedule of one call (everything but pointers and maps);
-// returns the grid size.  kv_splits > 1 cuts every item's key range into that
-// many slices, each a work item of its own.
+// returns the grid size (at most ctas_per_sm(d) CTAs per SM).  kv_splits > 1
+// cuts every item's key range into that many slices, each a work item of its
+// own.
 int setup_params(fa::FwdParams &p, int B, int H, int Nq, int Nk, int d, float scale, int causal, int sms,
                  int kv_splits = 1) {
     std::memset(&p, 0, sizeof p);
@@ -149,7 +155,8 @@ int setup_params(fa::FwdParams &p, int B, int H, int Nq, int Nk, int d, float sc
     p.Nq = Nq;
     p.Nk = Nk;
     p.Tr = (Nq + fa::kBR - 1) / fa::kBR;
-    p.Tc = (Nk + fa::kBC - 1) / fa::kBC;
+    p.bc = fa::kv_tile_keys(d);
+    p.Tc = (Nk + p.bc - 1) / p.bc;
     p.P = (p.Tr + 1) / 2;
     p.causal = causal != 0;
     // c2 = scale * log2(e).  A zero scale is run as the smallest normal float:
@@ -166,9 +173,10 @@ int setup_params(fa::FwdParams &p, int B, int H, int Nq, int Nk, int d, float sc
         p.n_pair_items = static_cast<int>(NP);
         p.n_items = static_cast<int>(NP * p.kv_splits);
     } else {
-        plan_schedule(p, sms);
+        plan_schedule(p, ctas_per_sm(d) * sms);
     }
-    return p.n_items < sms ? p.n_items : sms;
+    const int ctas = ctas_per_sm(d) * sms;
+    return p.n_items < ctas ? p.n_items : ctas;
 }
 
 // Key-range slices for the split path.  Splitting costs a partial write, a
@@ -176,11 +184,13 @@ int setup_params(fa::FwdParams &p, int B, int H, int Nq, int Nk, int d, float sc
 // leaves most SMs idle (at most half of them busy); then as many slices as
 // keep all items in one round (items <= SMs: a second, partial round would
 // double the time), never more slices than K/V tiles, at most 64.
-int choose_splits(int64_t BH, int Nq, int Nk, int sms) {
+int choose_splits(int64_t BH, int Nq, int Nk, int d, int sms) {
+    const int64_t ctas = static_cast<int64_t>(ctas_per_sm(d)) * sms;
     const int64_t pairs = BH * ((Nq + 2 * fa::kBR - 1) / (2 * fa::kBR));
-    if (2 * pairs > sms) return 1;
-    const int64_t tc = (Nk + fa::kBC - 1) / fa::kBC;
-    int64_t s = static_cast<int64_t>(sms) / pairs;
+    if (2 * pairs > ctas) return 1;
+    const int bc = fa::kv_tile_keys(d);
+    const int64_t tc = (Nk + bc - 1) / bc;
+    int64_t s = ctas / pairs;
     if (s > tc) s = tc;
     if (s > 64) s = 64;
     return s < 1 ? 1 : static_cast<int>(s);
@@ -208,12 +218,15 @@ template <int D, int MODE>
 fa_status launch(const fa::FwdParams &p, int grid, cudaStream_t stream, bool &attr_done) {
     using C = fa::Config<D, (MODE & fa::kFp8) != 0>;
     if (!attr_done) {
+        // the whole shared memory as carveout, so that kCtasPerSm CTAs fit an SM
         if (cudaFuncSetAttribute(fa::fa_fwd_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::kSmemBytes) != cudaSuccess)
+                                 C::kSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(fa::fa_fwd_kernel<D, MODE>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 100) != cudaSuccess)
             return FA_ERR_CUDA;
         attr_done = true;
     }
-    fa::fa_fwd_kernel<D, MODE><<<grid, fa::kThreads, C::kSmemBytes, stream>>>(p);
+    fa::fa_fwd_kernel<D, MODE><<<grid, C::kThreads, C::kSmemBytes, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -253,7 +266,8 @@ fa_status run_forward(const void *Q, const void *K, const void *V, void *O, floa
     fa::FwdParams p;
     const int grid = setup_params(p, B, H, Nq, Nk, d, scale, causal, sms, kv_splits);
     const int64_t BH = static_cast<int64_t>(B) * H;
-    if (!make_map(&p.tmQ, Q, BH, Nq, d) || !make_map(&p.tmK, K, BH, Nk, d) || !make_map(&p.tmV, V, BH, Nk, d))
+    if (!make_map(&p.tmQ, Q, BH, Nq, d) || !make_map(&p.tmK, K, BH, Nk, d, p.bc) ||
+        !make_map(&p.tmV, V, BH, Nk, d, p.bc))
         return FA_ERR_CUDA;
     p.O = static_cast<__nv_bfloat16 *>(O);
     p.LSE = LSE;
@@ -374,7 +388,7 @@ extern "C" fa_status fa_splitkv_workspace(int B, int H, int Nq, int Nk, int d, i
         DeviceInfo *info;
         st = device_info(sms, info);
         if (st != FA_OK) return st;
-        *num_splits = choose_splits(BH, Nq, Nk, sms);
+        *num_splits = choose_splits(BH, Nq, Nk, d, sms);
     }
     if (*num_splits > 256) return FA_ERR_INVALID_ARG;
     *bytes = splitkv_bytes(BH, Nq, d, *num_splits);
@@ -694,7 +708,7 @@ extern "C" fa_status fa_fwd_splitkv_noalloc(const void *Q, const void *K, const 
         DeviceInfo *info;
         st = device_info(sms, info);
         if (st != FA_OK) return st;
-        num_splits = choose_splits(BH, Nq, Nk, sms);
+        num_splits = choose_splits(BH, Nq, Nk, d, sms);
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (num_splits == 1)   // one slice: no partials, no scratch

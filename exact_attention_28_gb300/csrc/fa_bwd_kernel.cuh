@@ -353,33 +353,33 @@ __device__ void dkdv_mma_role(const BwdParams &p, const BwdShared &sh, uint32_t 
     if (!wait_bar(sh.first, 0, sh.abort_flag, 10, blockIdx.x, -1)) return;
     if (!wait_bar(sh.loadA0, 0, sh.abort_flag, 10, blockIdx.x, 0)) return;
     ptx::tc_fence_after_sync();
-    issue_s<D>(tST, sK, sQ0);        // S^T(0) = K Q_0^T
+    issue_s<D, kBC>(tST, sK, sQ0);        // S^T(0) = K Q_0^T
     ptx::mma_commit(sh.sfull);
     if (!wait_bar(sh.loadB0, 0, sh.abort_flag, 10, blockIdx.x, 0)) return;
     ptx::tc_fence_after_sync();
-    issue_s<D>(tdPT, sV, sdO0);      // dP^T(0) = V dO_0^T
+    issue_s<D, kBC>(tdPT, sV, sdO0);      // dP^T(0) = V dO_0^T
     ptx::mma_commit(sh.dpfull);
     for (int n = 0; n < n_i; ++n) {
         const int a = n % kSlotsA, b = n % kSlotsB;
         const int an = (n + 1) % kSlotsA, bn = (n + 1) % kSlotsB;
         if (!wait_bar(sh.pready, n & 1, sh.abort_flag, 11, blockIdx.x, n)) return;
         ptx::tc_fence_after_sync();
-        issue_pv<D>(tdV, tST, sdO0 + b * C::kTile, n > 0);    // dV += P^T dO_n
+        issue_pv<D, kBC>(tdV, tST, sdO0 + b * C::kTile, n > 0);    // dV += P^T dO_n
         ptx::mma_commit(sh.freeB0 + 8 * b);                   // dO_n read for the last time
         if (n + 1 < n_i) {
             if (!wait_bar(sh.loadA0 + 8 * an, ((n + 1) / kSlotsA) & 1, sh.abort_flag, 12, blockIdx.x, n + 1)) return;
             ptx::tc_fence_after_sync();
-            issue_s<D>(tST, sK, sQ0 + an * C::kTile);         // S^T(n+1)
+            issue_s<D, kBC>(tST, sK, sQ0 + an * C::kTile);         // S^T(n+1)
             ptx::mma_commit(sh.sfull);
         }
         if (!wait_bar(sh.dsready, n & 1, sh.abort_flag, 13, blockIdx.x, n)) return;
         ptx::tc_fence_after_sync();
-        issue_pv<D>(tdK, tdPT, sQ0 + a * C::kTile, n > 0);    // dK += dS^T Q_n
+        issue_pv<D, kBC>(tdK, tdPT, sQ0 + a * C::kTile, n > 0);    // dK += dS^T Q_n
         ptx::mma_commit(sh.freeA0 + 8 * a);                   // Q_n read for the last time
         if (n + 1 < n_i) {
             if (!wait_bar(sh.loadB0 + 8 * bn, ((n + 1) / kSlotsB) & 1, sh.abort_flag, 14, blockIdx.x, n + 1)) return;
             ptx::tc_fence_after_sync();
-            issue_s<D>(tdPT, sV, sdO0 + bn * C::kTile);       // dP^T(n+1)
+            issue_s<D, kBC>(tdPT, sV, sdO0 + bn * C::kTile);       // dP^T(n+1)
             ptx::mma_commit(sh.dpfull);
         }
     }
@@ -515,11 +515,11 @@ __device__ void dq_mma_role(const BwdParams &p, const BwdShared &sh, uint32_t tm
     if (!wait_bar(sh.first, 0, sh.abort_flag, 20, blockIdx.x, -1)) return;
     if (!wait_bar(sh.loadA0, 0, sh.abort_flag, 20, blockIdx.x, 0)) return;
     ptx::tc_fence_after_sync();
-    issue_s<D>(tS, sQ, sK0);        // S(0) = Q K_0^T
+    issue_s<D, kBC>(tS, sQ, sK0);        // S(0) = Q K_0^T
     ptx::mma_commit(sh.sfull);
     if (!wait_bar(sh.loadB0, 0, sh.abort_flag, 20, blockIdx.x, 0)) return;
     ptx::tc_fence_after_sync();
-    issue_s<D>(tdP, sdO, sV0);      // dP(0) = dO V_0^T
+    issue_s<D, kBC>(tdP, sdO, sV0);      // dP(0) = dO V_0^T
     ptx::mma_commit(sh.dpfull);
     ptx::mma_commit(sh.freeB0);     // V_0 read for the last time
     for (int n = 0; n < n_j; ++n) {
@@ -529,17 +529,17 @@ __device__ void dq_mma_role(const BwdParams &p, const BwdShared &sh, uint32_t tm
         if (n + 1 < n_j) {
             if (!wait_bar(sh.loadA0 + 8 * an, ((n + 1) / kSlotsA) & 1, sh.abort_flag, 22, blockIdx.x, n + 1)) return;
             ptx::tc_fence_after_sync();
-            issue_s<D>(tS, sQ, sK0 + an * C::kTile);          // S(n+1)
+            issue_s<D, kBC>(tS, sQ, sK0 + an * C::kTile);          // S(n+1)
             ptx::mma_commit(sh.sfull);
         }
         if (!wait_bar(sh.dsready, n & 1, sh.abort_flag, 23, blockIdx.x, n)) return;
         ptx::tc_fence_after_sync();
-        issue_pv<D>(tdQ, tdP, sK0 + a * C::kTile, n > 0);     // dQ += dS K_n
+        issue_pv<D, kBC>(tdQ, tdP, sK0 + a * C::kTile, n > 0);     // dQ += dS K_n
         ptx::mma_commit(sh.freeA0 + 8 * a);                   // K_n read for the last time
         if (n + 1 < n_j) {
             if (!wait_bar(sh.loadB0 + 8 * bn, ((n + 1) / kSlotsB) & 1, sh.abort_flag, 24, blockIdx.x, n + 1)) return;
             ptx::tc_fence_after_sync();
-            issue_s<D>(tdP, sdO, sV0 + bn * C::kTile);        // dP(n+1)
+            issue_s<D, kBC>(tdP, sdO, sV0 + bn * C::kTile);        // dP(n+1)
             ptx::mma_commit(sh.dpfull);
             ptx::mma_commit(sh.freeB0 + 8 * bn);              // V_{n+1} read for the last time
         }

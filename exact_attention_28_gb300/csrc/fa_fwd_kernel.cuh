@@ -17,21 +17,23 @@
 // items (causal) even out.  Items come in groups of heads whose K/V fit in
 // L2 together, heaviest first inside a group.
 //
-// Roles inside a CTA (384 threads, 3 warpgroups):
+// Roles inside a CTA (head dimension 128: 384 threads, 3 warpgroups; head
+// dimension 64: 320 threads, two CTAs per SM):
 //   warps 0-3   softmax for Q tile 0 (TMEM lanes 0-127: thread = query row)
 //   warps 4-7   softmax for Q tile 1
 //   warp  8     TMA producer: Q tiles once per item, then K_j, V_j into a ring
 //   warp  9     MMA issuer (one thread) and TMEM owner
-//   warps 10-11 idle (they complete the third warpgroup)
-// The softmax warpgroups raise their register limit to 208 (128 scores per
-// thread plus room for many exponentials in flight); the third warpgroup
-// lowers its own to 88.
+//   warps 10-11 idle at head dimension 128 (they complete the third warpgroup)
+// At head dimension 128 the softmax warpgroups raise their register limit to
+// 208 (128 scores per thread plus room for many exponentials in flight); the
+// third warpgroup lowers its own to 88.
 //
-// Tensor memory (512 columns x 128 lanes, fp32 cells):
-//   [  0,128)  S_0 = Q_0 K_j^T (fp32);  P_0 (bf16 pairs) overwrites its first 64 columns
-//   [128,256)  S_1 / P_1
-//   [256,256+D)      O_0 accumulator
-//   [256+D,256+2D)   O_1 accumulator
+// Tensor memory (BC = keys per K/V tile: 128 at d = 128, 64 at d = 64; fp32 cells):
+//   [0, BC)          S_0 = Q_0 K_j^T (fp32);  P_0 (bf16 pairs) overwrites its first BC/2 columns
+//   [BC, 2BC)        S_1 / P_1
+//   [2BC, 2BC+D)     O_0 accumulator
+//   [2BC+D, 2BC+2D)  O_1 accumulator
+// (512 columns at d = 128; 256 at d = 64, so that two CTAs fit an SM.)
 //
 // MMA order per KV step j (tile t = 0, 1):  PV_0(j), S_0(j+1), PV_1(j), S_1(j+1).
 // While the tensor core runs the other tile's two MMAs, the softmax warps of
@@ -55,15 +57,15 @@
 namespace fa {
 
 constexpr int kBR = 128;          // query rows per Q tile (= TMEM lanes)
-constexpr int kBC = 128;          // keys per K/V tile
-constexpr int kThreads = 384;     // 12 warps = 3 warpgroups
+constexpr int kBC = 128;          // keys per K/V tile of the backward (the forward's is Config::kBC)
 constexpr int kSoftmaxWarps = 8;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr uint32_t kSoftmaxRegs = 208;  // after setmaxnreg; launch gives 168
+// d = 128 (384 threads, one CTA per SM, 168 registers per thread at launch):
+constexpr uint32_t kSoftmaxRegs = 208;  // after setmaxnreg
 constexpr uint32_t kOtherRegs = 88;     // producer / MMA warpgroup
-static_assert(kSoftmaxRegs * 256 + kOtherRegs * 128 <= 168 * kThreads, "register split exceeds the launch allocation");
-constexpr int kChunkBytes = 128 * 128;  // one [128 rows x 64 bf16] swizzled TMA box
+static_assert(kSoftmaxRegs * 256 + kOtherRegs * 128 <= 168 * 384, "register split exceeds the launch allocation");
+constexpr int kChunkBytes = 128 * 128;  // one [128 rows x 64 bf16] swizzled TMA box (backward)
 constexpr float kTau = 8.0f;            // log2-domain slack before the max is raised
 // E4M3 P: a smaller slack and a headroom, p = 2^(c*s - m + 4) in (0, 2^8]:
 // the row maximum's weight lands in [2^4, 2^8] (E4M3 reaches 448), so keys
@@ -87,15 +89,29 @@ __device__ unsigned int g_fa_status;
 // First failure: {block, role, item, step}.
 __device__ int g_fa_diag[4];
 
-// Tile geometry.  bf16: a [128 rows][D] tile is D/64 boxes of [128][64].
+// Tile geometry.  bf16: a [rows][D] tile is D/64 boxes of [rows][64].
 // E4M3 (D = 128 only): a Q or K tile is one box of [128 rows][128 bytes] and
 // a V tile is V^T's [D channel rows][128 keys], also one box.
+//
+// Head dimension 128: K/V tiles of BC = 128 keys, one CTA of 384 threads per
+// SM holding 512 TMEM columns (S_0, S_1 of 128 columns, O_0, O_1 of 128).
+// Head dimension 64: K/V tiles of BC = 64 keys, so one CTA needs only 256
+// TMEM columns (S 64 + 64, O 64 + 64) and about 100 KB of shared memory, and
+// two CTAs share each SM: four query tiles' softmax warps per SM instead of
+// two, which hides the latency of each tile's softmax step behind the other
+// tiles' work (at d = 64 a tile's GEMMs are too short to hide it alone).
 template <int D, bool F8 = false>
 struct Config {
     static_assert(D == 64 || D == 128, "head dimension");
     static_assert(!F8 || D == 128, "the E4M3 path has D = 128 (one 128-byte row per tile row)");
     static constexpr int kElem = F8 ? 1 : 2;
-    static constexpr int kChunks = D * kElem / 128;        // 128-byte swizzle chunks per row
+    static constexpr int kBC = D == 64 ? 64 : 128;          // keys per K/V tile
+    static constexpr int kCtasPerSm = D == 64 ? 2 : 1;
+    static constexpr int kThreads = D == 64 ? 320 : 384;    // d = 64: no idle warps, no register split
+    static constexpr bool kRegSplit = D == 128;             // setmaxnreg between the warpgroups
+    static constexpr int kChunks = D * kElem / 128;         // 128-byte swizzle chunks per row
+    static constexpr int kQChunkBytes = kBR * 128;          // one [128 rows][128 B] box
+    static constexpr int kKVChunkBytes = kBC * 128;         // one [BC rows][128 B] box
     static constexpr int kQTileBytes = kBR * D * kElem;
     static constexpr int kKVTileBytes = kBC * D * kElem;
     static constexpr int kSlots = F8 ? 10 : (D == 128 ? 5 : 8);   // K/V ring depth (tiles)
@@ -103,14 +119,18 @@ struct Config {
     static constexpr int kRingBytes = kSlots * kKVTileBytes;
     static constexpr int kBarOffset = kQBytes + kRingBytes;
     static constexpr int kSmemBytes = kBarOffset + 256 + 1024;  // + barriers, + alignment slack
+    static_assert(kSmemBytes * kCtasPerSm + 1024 * kCtasPerSm <= 233472,
+                  "the CTAs of one SM exceed its 228 KB of shared memory");
     static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
-    static constexpr uint32_t kIdescS =
-        F8 ? ptx::instr_desc_e4m3_f32(kBR, kBC) : ptx::instr_desc_bf16_f32(kBR, kBC, false, false);
-    // bf16: V [keys][D] is an MN-major B operand; E4M3: V^T [D][keys] is K-major
-    static constexpr uint32_t kIdescPV =
-        F8 ? ptx::instr_desc_e4m3_f32(kBR, D) : ptx::instr_desc_bf16_f32(kBR, D, false, true);
-    static constexpr uint32_t kTmemCols = 512;
+    // TMEM columns: S_t at t * BC (P_t, bf16 pairs, over its first BC / 2
+    // columns), O_t at 2 * BC + t * D
+    static constexpr uint32_t kTmemCols = 2 * kBC + 2 * D;
+    static constexpr uint32_t kTmemS = 0, kTmemO = 2 * kBC;
+    static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation is a power of two");
 };
+
+// Keys per K/V tile for head dimension d (the host's view of Config::kBC).
+__host__ __device__ constexpr int kv_tile_keys(int d) { return d == 64 ? Config<64>::kBC : Config<128>::kBC; }
 
 struct FwdParams {
     CUtensorMap tmQ;   // [BH][Nq][D] bf16, box {64, 128, 1}, 128-byte swizzle
@@ -120,7 +140,8 @@ struct FwdParams {
     float *LSE;        // [BH][Nq]
     int BH, Nq, Nk;
     int Tr;            // Q tiles per head = ceil(Nq / 128)
-    int Tc;            // K/V tiles per head = ceil(Nk / 128)
+    int bc;            // keys per K/V tile (Config<D>::kBC)
+    int Tc;            // K/V tiles per head = ceil(Nk / bc)
     int P;             // Q-tile pairs per head = ceil(Tr / 2)
     int n_pair_items;  // items [0, n_pair_items) are whole pairs
     int n_items;       // the rest are single tiles of the last pairs in order
@@ -193,7 +214,7 @@ __host__ __device__ __forceinline__ Item decode_item(const FwdParams &p, int w, 
             if (p.causal) {
                 const int q_end_raw = it.q0 + (t + 1) * kBR;
                 const int q_end = q_end_raw < p.Nq ? q_end_raw : p.Nq;   // rows >= Nq are padding
-                const int need = (q_end - 1) / kBC + 1;
+                const int need = (q_end - 1) / p.bc + 1;
                 nk = need < p.Tc ? need : p.Tc;
             }
         }
@@ -241,7 +262,7 @@ __device__ __forceinline__ Item resolve_item(const FwdParams &p, int w) {
                 const int q_end = min(p.Nq, it.q0 + (t + 1) * kBR);
                 keys = min(seq, q_end + it.q_shift);
             }
-            vis[t] = keys > 0 ? (keys + kBC - 1) / kBC : 0;
+            vis[t] = keys > 0 ? (keys + p.bc - 1) / p.bc : 0;
         }
         if constexpr ((MODE & kSplit) != 0) {
             const int nkv = max(vis[0], vis[1]);
@@ -258,33 +279,37 @@ __device__ __forceinline__ Item resolve_item(const FwdParams &p, int w) {
     }
 }
 
-// Paged cache: a 128-key tile is read as kBC / rows boxes of rows =
-// min(block_size, 128) keys, box s from one page.  page_of_box gives that
+// Paged cache: a BC-key tile is read as BC / rows boxes of rows =
+// min(block_size, BC) keys, box s from one page.  page_of_box gives that
 // page for tile j of sequence b, or -1 when it is unallocated or past the
 // table (keys past the table lie beyond the sequence and are masked anyway).
+template <int BC>
 __device__ __forceinline__ int page_of_box(const FwdParams &p, int b, int j, int s, int rows) {
-    const int lp = (j * kBC + s * rows) / p.block_size;
+    const int lp = (j * BC + s * rows) / p.block_size;
     return lp < p.max_blocks ? __ldg(p.block_table + static_cast<size_t>(b) * p.max_blocks + lp) : -1;
 }
 
 // The pages of all boxes of tile j (at most 8: block_size >= 16).
+template <int BC>
 __device__ __forceinline__ void pages_of_tile(const FwdParams &p, int b, int j, int rows, int (&pg)[8]) {
     #pragma unroll
-    for (int s = 0; s < 8; ++s) pg[s] = s * rows < kBC ? page_of_box(p, b, j, s, rows) : 0;
+    for (int s = 0; s < 8; ++s) pg[s] = s * rows < BC ? page_of_box<BC>(p, b, j, s, rows) : 0;
 }
 
-// Loads one 128-key tile of the paged cache from the pages pg.  An
-// unallocated page is read from block 0 (its keys are masked by the softmax).
+// Loads one BC-key tile of the paged cache from the pages pg (chunks of
+// BC rows x 128 bytes).  An unallocated page is read from block 0 (its keys
+// are masked by the softmax).
+template <int BC>
 __device__ __forceinline__ void tma_load_paged_tile(const FwdParams &p, const CUtensorMap *map, uint32_t dst,
                                                     uint32_t bar, int h, int j, int rows, const int (&pg)[8],
                                                     int chunks, uint64_t pol) {
     #pragma unroll
     for (int s = 0; s < 8; ++s) {
-        if (s * rows >= kBC) break;
+        if (s * rows >= BC) break;
         const int phy = pg[s] < 0 ? 0 : pg[s];
-        const int row0 = (j * kBC + s * rows) % p.block_size;
+        const int row0 = (j * BC + s * rows) % p.block_size;
         for (int c = 0; c < chunks; ++c)
-            ptx::tma_load_4d(dst + c * kChunkBytes + s * rows * 128, map, bar, c * 64, row0, h, phy, pol);
+            ptx::tma_load_4d(dst + c * BC * 128 + s * rows * 128, map, bar, c * 64, row0, h, phy, pol);
     }
 }
 
@@ -366,21 +391,21 @@ __device__ void producer_role(const FwdParams &p, const Shared &sh, uint32_t sme
         for (int t = 0; t < item.ntiles; ++t)
             #pragma unroll
             for (int c = 0; c < C::kChunks; ++c)
-                ptx::tma_load_3d(smem_q + t * C::kQTileBytes + c * kChunkBytes, &p.tmQ, sh.q_full,
+                ptx::tma_load_3d(smem_q + t * C::kQTileBytes + c * C::kQChunkBytes, &p.tmQ, sh.q_full,
                                  c * 64, item.q0 + t * kBR, item.bh, pol_q);
         const int nkv = max(item.nk[0], item.nk[1]);
         // paged: the pages of tile j (pg) and of tile j + 1 (pg_next, fetched
         // one tile ahead so the table lookups do not delay the copies)
         [[maybe_unused]] int pg[8], pg_next[8];
-        [[maybe_unused]] const int rows = p.block_size < kBC ? p.block_size : kBC;
+        [[maybe_unused]] const int rows = p.block_size < C::kBC ? p.block_size : C::kBC;
         if constexpr ((MODE & kPaged) != 0)
-            if (item.kv0 < nkv) pages_of_tile(p, item.bh / p.H, item.kv0, rows, pg_next);
+            if (item.kv0 < nkv) pages_of_tile<C::kBC>(p, item.bh / p.H, item.kv0, rows, pg_next);
         bool ok = true;
         for (int j = item.kv0; j < nkv && ok; ++j) {
             if constexpr ((MODE & kPaged) != 0) {
                 #pragma unroll
                 for (int s = 0; s < 8; ++s) pg[s] = pg_next[s];
-                if (j + 1 < nkv) pages_of_tile(p, item.bh / p.H, j + 1, rows, pg_next);
+                if (j + 1 < nkv) pages_of_tile<C::kBC>(p, item.bh / p.H, j + 1, rows, pg_next);
             }
             #pragma unroll 1
             for (int which = 0; which < 2; ++which, ++it) {
@@ -395,17 +420,17 @@ __device__ void producer_role(const FwdParams &p, const Shared &sh, uint32_t sme
                 ptx::mbar_arrive_expect_tx(full, C::kKVTileBytes);
                 const CUtensorMap *map = which ? &p.tmV : &p.tmK;
                 if constexpr ((MODE & kPaged) != 0) {
-                    tma_load_paged_tile(p, map, smem_ring + slot * C::kKVTileBytes, full, item.bh % p.H, j, rows, pg,
+                    tma_load_paged_tile<C::kBC>(p, map, smem_ring + slot * C::kKVTileBytes, full, item.bh % p.H, j, rows, pg,
                                         C::kChunks, pol_kv);
                 } else if constexpr ((MODE & kFp8) != 0) {
                     // K: rows j*128.. of [Nk][128 B]; V^T: columns j*128.. of [D][ldn]
-                    ptx::tma_load_3d(smem_ring + slot * C::kKVTileBytes, map, full, which ? j * kBC : 0,
-                                     which ? 0 : j * kBC, item.bh, pol_kv);
+                    ptx::tma_load_3d(smem_ring + slot * C::kKVTileBytes, map, full, which ? j * C::kBC : 0,
+                                     which ? 0 : j * C::kBC, item.bh, pol_kv);
                 } else {
                     #pragma unroll
                     for (int c = 0; c < C::kChunks; ++c)
-                        ptx::tma_load_3d(smem_ring + slot * C::kKVTileBytes + c * kChunkBytes, map, full,
-                                         c * 64, j * kBC, item.bh, pol_kv);
+                        ptx::tma_load_3d(smem_ring + slot * C::kKVTileBytes + c * C::kKVChunkBytes, map, full,
+                                         c * 64, j * C::kBC, item.bh, pol_kv);
                 }
                 loads_issued = it + 1;
             }
@@ -416,51 +441,58 @@ __device__ void producer_role(const FwdParams &p, const Shared &sh, uint32_t sme
 
 // ----------------------------------------------------------------- MMA warp
 
-// S_t = Q_t K_j^T: D/16 MMAs of K = 16.  Q and K tiles are D/64 boxes of
-// [128 rows][64 cols], 128-byte swizzled; step kk reads columns 16kk..16kk+15,
-// i.e. box kk/4 at byte offset 32*(kk%4) inside each 128-byte row.
+// S_t = Q_t K_j^T: D/16 MMAs of K = 16, N = BC.  Q and K tiles are D/64
+// boxes of [128 or BC rows][64 cols], 128-byte swizzled; step kk reads
+// columns 16kk..16kk+15, i.e. box kk/4 at byte offset 32*(kk%4) inside each
+// 128-byte row.
 // E4M3: D/32 MMAs of K = 32, the same 32-byte steps inside the one chunk.
-template <int D, bool F8 = false>
+// (The backward calls it with BC = 128 for its transposed products.)
+template <int D, int BC, bool F8 = false>
 __device__ __forceinline__ void issue_s(uint32_t tmem_s, uint32_t q_tile, uint32_t k_tile) {
-    using C = Config<D, F8>;
+    constexpr int kElem = F8 ? 1 : 2;
+    constexpr uint32_t kIdesc =
+        F8 ? ptx::instr_desc_e4m3_f32(kBR, BC) : ptx::instr_desc_bf16_f32(kBR, BC, false, false);
     constexpr uint32_t hi = ptx::sdesc_sw128_hi(1024);
     const uint32_t a0 = ptx::sdesc_sw128_lo(q_tile, 16);
     const uint32_t b0 = ptx::sdesc_sw128_lo(k_tile, 16);
-    constexpr int kSteps = D * C::kElem / 32;
+    constexpr int kSteps = D * kElem / 32;
     #pragma unroll
     for (int kk = 0; kk < kSteps; ++kk) {
-        const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+        const uint32_t offa = ((kk >> 2) * (kBR * 128) + (kk & 3) * 32) >> 4;
+        const uint32_t offb = ((kk >> 2) * (BC * 128) + (kk & 3) * 32) >> 4;
         if constexpr (F8)
-            ptx::mma_f8_ss(tmem_s, a0 + off, hi, b0 + off, hi, C::kIdescS, kk > 0 ? 1u : 0u);
+            ptx::mma_f8_ss(tmem_s, a0 + offa, hi, b0 + offb, hi, kIdesc, kk > 0 ? 1u : 0u);
         else
-            ptx::mma_bf16_ss(tmem_s, a0 + off, hi, b0 + off, hi, C::kIdescS, kk > 0 ? 1u : 0u);
+            ptx::mma_bf16_ss(tmem_s, a0 + offa, hi, b0 + offb, hi, kIdesc, kk > 0 ? 1u : 0u);
     }
 }
 
-// O_t (+)= P_t V_j: 8 MMAs of K = 16 keys; P_t is read from TMEM (16 keys =
-// 8 columns of bf16 pairs per step).  V tile: [128 keys][D] as D/64 boxes of
-// [128][64]; the B operand is MN-major (D contiguous): 8-key groups SBO =
-// 1024 B apart, 64-column groups LBO = one box (16 KB) apart.
+// O_t (+)= P_t V_j: BC/16 MMAs of K = 16 keys; P_t is read from TMEM (16
+// keys = 8 columns of bf16 pairs per step).  V tile: [BC keys][D] as D/64
+// boxes of [BC][64]; the B operand is MN-major (D contiguous): 8-key groups
+// SBO = 1024 B apart, 64-column groups LBO = one box (BC * 128 B) apart.
 //
 // E4M3: 4 MMAs of K = 32 keys; P is 4 keys per TMEM column (8 columns per
 // step) and V^T [D rows][128 keys] is a K-major operand like K in S: 8-row
 // groups 1024 B apart, 32-byte steps along the keys.
-template <int D, bool F8 = false>
+template <int D, int BC, bool F8 = false>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_tile,
                                          bool accumulate) {
-    using C = Config<D, F8>;
+    // bf16: V [keys][D] is an MN-major B operand; E4M3: V^T [D][keys] is K-major
+    constexpr uint32_t kIdesc =
+        F8 ? ptx::instr_desc_e4m3_f32(kBR, D) : ptx::instr_desc_bf16_f32(kBR, D, false, true);
     constexpr uint32_t hi = ptx::sdesc_sw128_hi(1024);
     if constexpr (F8) {
         const uint32_t b0 = ptx::sdesc_sw128_lo(v_tile, 16);
         #pragma unroll
-        for (int kk = 0; kk < kBC / 32; ++kk)
-            ptx::mma_f8_ts(tmem_o, tmem_p + kk * 8, b0 + ((kk * 32) >> 4), hi, C::kIdescPV,
+        for (int kk = 0; kk < BC / 32; ++kk)
+            ptx::mma_f8_ts(tmem_o, tmem_p + kk * 8, b0 + ((kk * 32) >> 4), hi, kIdesc,
                            (accumulate || kk > 0) ? 1u : 0u);
     } else {
-        const uint32_t b0 = ptx::sdesc_sw128_lo(v_tile, kChunkBytes);
+        const uint32_t b0 = ptx::sdesc_sw128_lo(v_tile, BC * 128);
         #pragma unroll
-        for (int kk = 0; kk < kBC / 16; ++kk)
-            ptx::mma_bf16_ts(tmem_o, tmem_p + kk * 8, b0 + ((kk * 16 * 128) >> 4), hi, C::kIdescPV,
+        for (int kk = 0; kk < BC / 16; ++kk)
+            ptx::mma_bf16_ts(tmem_o, tmem_p + kk * 8, b0 + ((kk * 16 * 128) >> 4), hi, kIdesc,
                              (accumulate || kk > 0) ? 1u : 0u);
     }
 }
@@ -472,8 +504,8 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
     using C = Config<D, F8>;
     uint32_t it = 0;
     uint32_t p_phase[2] = {0u, 0u};
-    const uint32_t tS[2] = {tmem + 0u, tmem + 128u};
-    const uint32_t tO[2] = {tmem + 256u, tmem + 256u + D};
+    const uint32_t tS[2] = {tmem + C::kTmemS, tmem + C::kTmemS + C::kBC};
+    const uint32_t tO[2] = {tmem + C::kTmemO, tmem + C::kTmemO + D};
     const uint32_t sQ[2] = {smem_q, smem_q + C::kQTileBytes};
     for (int k = 0;; ++k) {
         const int w = item_of_round(p, k);
@@ -502,7 +534,7 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
                 if (!wait_bar(ring_bar(ki), (ki / C::kSlots) & 1, sh.abort_flag, 1, w, jj)) return false;
                 ptx::tc_fence_after_sync();
                 const int buf = (jj - kv0) & 1;
-                issue_s<D, F8>(tS[buf], sQ[0], ring_tile(ki));
+                issue_s<D, C::kBC, F8>(tS[buf], sQ[0], ring_tile(ki));
                 ptx::mma_commit(buf ? sh.s_alt : sh.s_full0);
                 ptx::mma_commit(sh.kv_empty0 + 8 * (ki % C::kSlots));
                 return true;
@@ -516,7 +548,7 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
                 if (!wait_bar(sh.p_full0, p_phase[0], sh.abort_flag, 1, w, j)) return;
                 p_phase[0] ^= 1u;
                 ptx::tc_fence_after_sync();
-                issue_pv<D, F8>(tO[0], tS[(j - kv0) & 1], ring_tile(vi), j > kv0);
+                issue_pv<D, C::kBC, F8>(tO[0], tS[(j - kv0) & 1], ring_tile(vi), j > kv0);
                 ptx::mma_commit(j == nk0 - 1 ? sh.o_full0 : sh.pv_done);
                 ptx::mma_commit(sh.kv_empty0 + 8 * (vi % C::kSlots));
                 if (j + 2 < nk0) {
@@ -534,7 +566,7 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
         ptx::tc_fence_after_sync();
         for (int t = 0; t < 2; ++t) {
             if (item.nk[t] > kv0) {
-                issue_s<D, F8>(tS[t], sQ[t], smem_ring + ks * C::kKVTileBytes);
+                issue_s<D, C::kBC, F8>(tS[t], sQ[t], smem_ring + ks * C::kKVTileBytes);
                 ptx::mma_commit(sh.s_full0 + 8 * t);
             }
         }
@@ -555,7 +587,7 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
                 if (!wait_bar(sh.p_full0, p_phase[0], sh.abort_flag, 1, w, j)) return;
                 p_phase[0] ^= 1u;
                 ptx::tc_fence_after_sync();
-                issue_pv<D, F8>(tO[0], tS[0], v_tile, j > kv0);
+                issue_pv<D, C::kBC, F8>(tO[0], tS[0], v_tile, j > kv0);
                 if (j == nk0 - 1) ptx::mma_commit(sh.o_full0);
             }
             if (more) {
@@ -563,7 +595,7 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
                     return;
                 ptx::tc_fence_after_sync();
                 if (j + 1 < nk0) {
-                    issue_s<D, F8>(tS[0], sQ[0], smem_ring + ks2 * C::kKVTileBytes);
+                    issue_s<D, C::kBC, F8>(tS[0], sQ[0], smem_ring + ks2 * C::kKVTileBytes);
                     ptx::mma_commit(sh.s_full0);
                 }
             }
@@ -571,13 +603,13 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
                 if (!wait_bar(sh.p_full0 + 8, p_phase[1], sh.abort_flag, 1, w, j)) return;
                 p_phase[1] ^= 1u;
                 ptx::tc_fence_after_sync();
-                issue_pv<D, F8>(tO[1], tS[1], v_tile, j > kv0);
+                issue_pv<D, C::kBC, F8>(tO[1], tS[1], v_tile, j > kv0);
                 if (j == nk1 - 1) ptx::mma_commit(sh.o_full0 + 8);
             }
             ptx::mma_commit(sh.kv_empty0 + 8 * vs);
             if (more) {
                 if (j + 1 < nk1) {
-                    issue_s<D, F8>(tS[1], sQ[1], smem_ring + ks2 * C::kKVTileBytes);
+                    issue_s<D, C::kBC, F8>(tS[1], sQ[1], smem_ring + ks2 * C::kKVTileBytes);
                     ptx::mma_commit(sh.s_full0 + 8);
                 }
                 ptx::mma_commit(sh.kv_empty0 + 8 * ks2);
@@ -596,39 +628,45 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
 // row maximum is an in-register reduction and many exponentials of
 // independent pairs can be in flight together.
 
-// Row extreme (max for a positive scale, min for a negative one) of 128 scores.
-__device__ __forceinline__ float row_extreme128(const uint32_t (&s)[128], bool pos) {
+// Row extreme (max for a positive scale, min for a negative one) of N = 64
+// or 128 scores: eight independent three-input chains, then a short tree.
+template <int N>
+__device__ __forceinline__ float row_extreme(const uint32_t (&s)[N], bool pos) {
+    static_assert(N == 64 || N == 128, "row length");
     float a[8];
     #pragma unroll
     for (int i = 0; i < 8; ++i) a[i] = __uint_as_float(s[i]);
     if (pos) {
         #pragma unroll
-        for (int c = 8; c < 120; c += 16)
+        for (int c = 8; c + 16 <= N - 8; c += 16)
             #pragma unroll
             for (int i = 0; i < 8; ++i)
                 a[i] = ptx::max3(a[i], __uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1]));
         #pragma unroll
-        for (int i = 0; i < 4; ++i) a[i] = ptx::max3(a[i], __uint_as_float(s[120 + 2 * i]), __uint_as_float(s[121 + 2 * i]));
+        for (int i = 0; i < 4; ++i)
+            a[i] = ptx::max3(a[i], __uint_as_float(s[N - 8 + 2 * i]), __uint_as_float(s[N - 7 + 2 * i]));
         return fmaxf(ptx::max3(a[0], a[1], a[2]), ptx::max3(a[3], ptx::max3(a[4], a[5], a[6]), a[7]));
     }
     #pragma unroll
-    for (int c = 8; c < 120; c += 16)
+    for (int c = 8; c + 16 <= N - 8; c += 16)
         #pragma unroll
         for (int i = 0; i < 8; ++i)
             a[i] = ptx::min3(a[i], __uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1]));
     #pragma unroll
-    for (int i = 0; i < 4; ++i) a[i] = ptx::min3(a[i], __uint_as_float(s[120 + 2 * i]), __uint_as_float(s[121 + 2 * i]));
+    for (int i = 0; i < 4; ++i)
+        a[i] = ptx::min3(a[i], __uint_as_float(s[N - 8 + 2 * i]), __uint_as_float(s[N - 7 + 2 * i]));
     return fminf(ptx::min3(a[0], a[1], a[2]), ptx::min3(a[3], ptx::min3(a[4], a[5], a[6]), a[7]));
 }
 
-// P for the row's 128 scores: p = 2^(c*s - m), packed to bf16 pairs (round
-// to nearest even) and stored over the first 64 TMEM columns of the S tile.
+// P for the row's N scores: p = 2^(c*s - m), packed to bf16 pairs (round
+// to nearest even) and stored over the first N/2 TMEM columns of the S tile.
 // Row sums: of the fp32 p (for LSE) and of the bf16 p that P V actually
 // uses, which normalises O: the weights then sum to one exactly, so a
 // dominant key carries no rounding error into O.  Masked keys hold
 // -inf*sign(c) and come out as p = 0.
-__device__ __forceinline__ void exp_pack_store128(const uint32_t (&s)[128], float c2, float neg_m, uint32_t tP,
-                                                  float &sum_exact, float &sum_rounded) {
+template <int N>
+__device__ __forceinline__ void exp_pack_store(const uint32_t (&s)[N], float c2, float neg_m, uint32_t tP,
+                                               float &sum_exact, float &sum_rounded) {
     const uint64_t c2x2 = ptx::f2_pack(c2, c2), mx2 = ptx::f2_pack(neg_m, neg_m);
     uint64_t acc_e[4];
     #pragma unroll
@@ -636,9 +674,9 @@ __device__ __forceinline__ void exp_pack_store128(const uint32_t (&s)[128], floa
     float r[8];
     #pragma unroll
     for (int i = 0; i < 8; ++i) r[i] = 0.f;
-    uint32_t pk[64];
+    uint32_t pk[N / 2];
     #pragma unroll
-    for (int i = 0; i < 64; ++i) {
+    for (int i = 0; i < N / 2; ++i) {
         const uint64_t t = ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
                                        c2x2, mx2);
         float t0, t1;
@@ -649,7 +687,7 @@ __device__ __forceinline__ void exp_pack_store128(const uint32_t (&s)[128], floa
         ptx::add_bf16x2_to_f32(r[2 * (i & 3)], r[2 * (i & 3) + 1], pk[i]);
     }
     #pragma unroll
-    for (int q = 0; q < 4; ++q)
+    for (int q = 0; q < N / 32; ++q)
         ptx::tmem_store_16cols(tP + 16 * q, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * q]));
     float e0, e1;
     ptx::f2_unpack(ptx::f2_add(ptx::f2_add(acc_e[0], acc_e[1]), ptx::f2_add(acc_e[2], acc_e[3])), e0, e1);
@@ -695,19 +733,21 @@ __device__ __forceinline__ void exp_pack_store128_e4m3(const uint32_t (&s)[128],
 
 template <int D, int MODE>
 __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem, int tile, int quad, int lane) {
+    constexpr bool F8 = (MODE & kFp8) != 0;
+    using C = Config<D, F8>;
+    constexpr int BC = C::kBC;
     const int row = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t tS = tmem + lane_off + tile * 128;
-    const uint32_t tO = tmem + lane_off + 256 + tile * D;
-    constexpr bool F8 = (MODE & kFp8) != 0;
+    const uint32_t tS = tmem + lane_off + C::kTmemS + tile * BC;
+    const uint32_t tO = tmem + lane_off + C::kTmemO + tile * D;
     float c2 = p.c2;
     const bool pos = c2 > 0.f;   // the descales are positive: the sign is the scale's
     // A masked key must never win the row extreme and must give p = 0:
     // -inf for a positive scale, +inf for a negative one (the host never
     // passes c2 == 0, see fa_fwd).
     const float mask_val = pos ? -INFINITY : INFINITY;
-    // paged: keys per box (min(block_size, 128)) and its log2
-    [[maybe_unused]] const int page_rows = p.block_size < kBC ? p.block_size : kBC;
+    // paged: keys per box (min(block_size, BC)) and its log2
+    [[maybe_unused]] const int page_rows = p.block_size < BC ? p.block_size : BC;
     [[maybe_unused]] const int page_shift = (MODE & kPaged) != 0 ? 31 - __clz(page_rows) : 0;
     uint32_t s_phase = 0, o_phase = 0;
     uint32_t sa_phase = 0, pv_phase = 0;   // single-tile items (tile 0 only)
@@ -755,10 +795,10 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
             // wait, so the load overlaps it
             [[maybe_unused]] int box_page = 0;
             if constexpr ((MODE & kPaged) != 0)
-                if (lane * page_rows < kBC) box_page = page_of_box(p, item.bh / p.H, j, lane, page_rows);
+                if (lane * page_rows < BC) box_page = page_of_box<BC>(p, item.bh / p.H, j, lane, page_rows);
             // single-tile items alternate S buffers (the second is tile 1's region)
             const bool alt = single && ((j - item.kv0) & 1);
-            const uint32_t tSj = tS + (alt ? 128u : 0u);
+            const uint32_t tSj = tS + (alt ? static_cast<uint32_t>(BC) : 0u);
             if (alt) {
                 if (!wait_bar(sh.s_alt, sa_phase, sh.abort_flag, 2, w, j)) return;
                 sa_phase ^= 1u;
@@ -767,32 +807,35 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
                 s_phase ^= 1u;
             }
             ptx::tc_fence_after_sync();
-            uint32_t s[128];
-            ptx::tmem_load_128cols(tSj, s);
-            const int kvalid = key_lim - j * kBC;
+            uint32_t s[BC];
+            if constexpr (BC == 128)
+                ptx::tmem_load_128cols(tSj, s);
+            else
+                ptx::tmem_load_64cols(tSj, s);
+            const int kvalid = key_lim - j * BC;
             if constexpr ((MODE & kPaged) != 0) {
                 // bit s: box s lies in an unallocated page (warp-uniform)
                 const uint32_t holes = __ballot_sync(0xffffffffu, box_page < 0);
-                if (__any_sync(0xffffffffu, kvalid < kBC) || holes) {   // warp-uniform masked path
+                if (__any_sync(0xffffffffu, kvalid < BC) || holes) {   // warp-uniform masked path
                     // column mask, bit c % 32 of word c / 32 (a box holds >= 16 columns)
-                    uint32_t cm[4];
+                    uint32_t cm[BC / 32];
                     #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                    for (int q = 0; q < BC / 32; ++q) {
                         cm[q] = ((holes >> ((32 * q) >> page_shift)) & 1u) ? 0x0000FFFFu : 0u;
                         cm[q] |= ((holes >> ((32 * q + 16) >> page_shift)) & 1u) ? 0xFFFF0000u : 0u;
                     }
                     #pragma unroll
-                    for (int c = 0; c < 128; ++c)
+                    for (int c = 0; c < BC; ++c)
                         if (c >= kvalid || ((cm[c >> 5] >> (c & 31)) & 1u)) s[c] = __float_as_uint(mask_val);
                 }
             } else {
-                if (__any_sync(0xffffffffu, kvalid < kBC)) {   // warp-uniform masked path
+                if (__any_sync(0xffffffffu, kvalid < BC)) {   // warp-uniform masked path
                     #pragma unroll
-                    for (int c = 0; c < 128; ++c)
+                    for (int c = 0; c < BC; ++c)
                         if (c >= kvalid) s[c] = __float_as_uint(mask_val);
                 }
             }
-            const float mx = row_extreme128(s, pos);
+            const float mx = row_extreme<BC>(s, pos);
             const float m_tile = kvalid > 0 ? mx * c2 : -INFINITY;
             float alpha = 1.f;
             if (m_tile > m_ref + (F8 ? kTauF8 : kTau)) {
@@ -808,7 +851,7 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
             if constexpr (F8)
                 exp_pack_store128_e4m3(s, c2, m_ref == -INFINITY ? 0.f : kHeadroomF8 - m_ref, tSj, se, sr);
             else
-                exp_pack_store128(s, c2, m_ref == -INFINITY ? 0.f : -m_ref, tSj, se, sr);
+                exp_pack_store<BC>(s, c2, m_ref == -INFINITY ? 0.f : -m_ref, tSj, se, sr);
             l += se;
             l_rounded += sr;
             // single-tile items: S(j) ready no longer implies P(j-1) V done;
@@ -889,7 +932,8 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
 // ------------------------------------------------------------------- kernel
 
 template <int D, int MODE>
-__global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(Config<D>::kThreads, Config<D>::kCtasPerSm)
+    fa_fwd_kernel(const __grid_constant__ FwdParams p) {
     using C = Config<D, (MODE & kFp8) != 0>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte-swizzled operand tiles.
@@ -956,10 +1000,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 
     uint32_t loads_issued = 0, q_arms = 0;
     if (warp < kSoftmaxWarps) {
-        ptx::setmaxnreg_inc<kSoftmaxRegs>();
+        if constexpr (C::kRegSplit) ptx::setmaxnreg_inc<kSoftmaxRegs>();
         softmax_role<D, MODE>(p, sh, tmem, warp >> 2, warp & 3, lane);
     } else if (warp == kProducerWarp) {
-        ptx::setmaxnreg_dec<kOtherRegs>();
+        if constexpr (C::kRegSplit) ptx::setmaxnreg_dec<kOtherRegs>();
         if (lane == 0) {
             producer_role<D, MODE>(p, sh, smem_q, smem_ring, loads_issued, q_arms);
             // Drain: every copy this CTA started must land before it exits.
@@ -970,7 +1014,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         }
         __syncwarp();
     } else {
-        ptx::setmaxnreg_dec<kOtherRegs>();
+        if constexpr (C::kRegSplit) ptx::setmaxnreg_dec<kOtherRegs>();
         if (warp == kMmaWarp && lane == 0) mma_role<D, MODE>(p, sh, tmem, smem_q, smem_ring);
         __syncwarp();
     }

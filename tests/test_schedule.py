@@ -3,6 +3,8 @@
 Every (batch*head, 128-row query tile) must be computed exactly once, each
 with the key/value tiles its rows can see (all of them, or those up to the
 diagonal under the causal mask), and the rounds must balance across CTAs.
+Key/value tiles hold 128 keys at head dimension 128 and 64 keys at head
+dimension 64, where two persistent CTAs share each SM.
 """
 import math
 
@@ -29,9 +31,18 @@ def expand(items):
     return tiles
 
 
-def visible_tiles(Nq, Nk, causal, q):
-    Tc = math.ceil(Nk / 128)
-    return min(Tc, (min(Nq, q + 128) - 1) // 128 + 1) if causal else Tc
+def kv_keys(d):
+    return 64 if d == 64 else 128
+
+
+def ctas_per_sm(d):
+    return 2 if d == 64 else 1
+
+
+def visible_tiles(Nq, Nk, causal, q, d):
+    bc = kv_keys(d)
+    Tc = math.ceil(Nk / bc)
+    return min(Tc, (min(Nq, q + 128) - 1) // bc + 1) if causal else Tc
 
 
 SHAPES = [
@@ -52,12 +63,12 @@ def test_every_tile_exactly_once_with_its_kv_range(B, H, Nq, Nk, d, causal, sms)
     assert len(set((bh, q) for bh, q, *_ in tiles)) == B * H * Tr
     for bh, q, kv0, end, split in tiles:
         assert 0 <= bh < B * H and q % 128 == 0 and q < Nq and kv0 == 0 and split == 0
-        assert end == visible_tiles(Nq, Nk, causal, q), (bh, q, end)
+        assert end == visible_tiles(Nq, Nk, causal, q, d), (bh, q, end)
     # each CTA walks consecutive rounds 0, 1, 2, ...
     for cta in np.unique(items[:, 0]):
         rounds = np.sort(items[items[:, 0] == cta, 1])
         assert np.array_equal(rounds, np.arange(len(rounds)))
-    assert items[:, 0].max() < sms
+    assert items[:, 0].max() < ctas_per_sm(d) * sms
 
 
 @pytest.mark.parametrize("B,H,Nq,Nk,d,causal", SHAPES)
@@ -73,7 +84,7 @@ def test_key_slices_partition_each_tiles_range(B, H, Nq, Nk, d, causal, splits):
         covered = []
         for _, kv0, end in parts:
             covered.extend(range(kv0, max(kv0, end)))
-        assert sorted(covered) == list(range(visible_tiles(Nq, Nk, causal, q))), (bh, q)
+        assert sorted(covered) == list(range(visible_tiles(Nq, Nk, causal, q, d))), (bh, q)
 
 
 def cta_loads(items, key=lambda nk: 1):
