@@ -659,21 +659,17 @@ __device__ __forceinline__ float row_extreme(const uint32_t (&s)[N], bool pos) {
 }
 
 // P for the row's N scores: p = 2^(c*s - m), packed to bf16 pairs (round
-// to nearest even) and stored over the first N/2 TMEM columns of the S tile.
-// Row sums: of the fp32 p (for LSE) and of the bf16 p that P V actually
-// uses, which normalises O: the weights then sum to one exactly, so a
-// dominant key carries no rounding error into O.  Masked keys hold
-// -inf*sign(c) and come out as p = 0.
+// to nearest even) and stored over the first N/2 TMEM columns of the S tile;
+// returns the row sum of the fp32 p.  Masked keys hold -inf*sign(c) and come
+// out as p = 0.  (The sum that normalises O adds the bf16 rounding of each
+// tile's largest weight, see max_weight_rounding.)
 template <int N>
 __device__ __forceinline__ void exp_pack_store(const uint32_t (&s)[N], float c2, float neg_m, uint32_t tP,
-                                               float &sum_exact, float &sum_rounded) {
+                                               float &sum_exact) {
     const uint64_t c2x2 = ptx::f2_pack(c2, c2), mx2 = ptx::f2_pack(neg_m, neg_m);
     uint64_t acc_e[4];
     #pragma unroll
     for (int i = 0; i < 4; ++i) acc_e[i] = ptx::f2_pack(0.f, 0.f);
-    float r[8];
-    #pragma unroll
-    for (int i = 0; i < 8; ++i) r[i] = 0.f;
     uint32_t pk[N / 2];
     #pragma unroll
     for (int i = 0; i < N / 2; ++i) {
@@ -684,7 +680,6 @@ __device__ __forceinline__ void exp_pack_store(const uint32_t (&s)[N], float c2,
         const float p0 = ptx::ex2(t0), p1 = ptx::ex2(t1);
         acc_e[i & 3] = ptx::f2_add(acc_e[i & 3], ptx::f2_pack(p0, p1));
         pk[i] = ptx::pack_bf16x2(p0, p1);
-        ptx::add_bf16x2_to_f32(r[2 * (i & 3)], r[2 * (i & 3) + 1], pk[i]);
     }
     #pragma unroll
     for (int q = 0; q < N / 32; ++q)
@@ -692,7 +687,20 @@ __device__ __forceinline__ void exp_pack_store(const uint32_t (&s)[N], float c2,
     float e0, e1;
     ptx::f2_unpack(ptx::f2_add(ptx::f2_add(acc_e[0], acc_e[1]), ptx::f2_add(acc_e[2], acc_e[3])), e0, e1);
     sum_exact = e0 + e1;
-    sum_rounded = ((r[0] + r[1]) + (r[2] + r[3])) + ((r[4] + r[5]) + (r[6] + r[7]));
+}
+
+// bf16(p) - p for the weight p of the tile's extreme score mx, computed with
+// the arithmetic exp_pack_store applies to that key, so the result is the
+// exact rounding error P V sees on the row's largest weight of the tile.
+// O is normalised by the fp32 sum plus these errors: a row dominated by one
+// key then carries no 2^-9 relative bias into O (the weights of the other
+// keys are small, and their rounding errors average out).
+__device__ __forceinline__ float max_weight_rounding(float mx, float c2, float neg_m) {
+    float t, t1;
+    ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(mx, mx), ptx::f2_pack(c2, c2), ptx::f2_pack(neg_m, neg_m)), t, t1);
+    const float pmax = ptx::ex2(t);
+    const uint32_t pk = ptx::pack_bf16x2(pmax, pmax);
+    return __uint_as_float(pk << 16) - pmax;
 }
 
 // E4M3 P: the same exponentials, packed four keys to a TMEM column (32
@@ -788,7 +796,8 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
         }
         float m_ref = -INFINITY;   // log2-domain reference maximum
         float l = 0.f;             // sum of p (fp32), for LSE
-        float l_rounded = 0.f;     // sum of the bf16 p that P V uses, for O
+        float l_rounded = 0.f;     // the sum that normalises O (E4M3: of the rounded p;
+                                   // bf16: the rounding of each tile's largest weight, added to l)
 
         for (int j = item.kv0; j < nk; ++j) {
             // paged: lane s looks up the page of box s of this tile before the
@@ -847,13 +856,18 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
 
             // m_ref is finite once a row has seen a key (every row sees key 0
             // in its first tile); the guard keeps a fully masked row at p = 0.
-            float se, sr;
-            if constexpr (F8)
+            if constexpr (F8) {
+                float se, sr;
                 exp_pack_store128_e4m3(s, c2, m_ref == -INFINITY ? 0.f : kHeadroomF8 - m_ref, tSj, se, sr);
-            else
-                exp_pack_store<BC>(s, c2, m_ref == -INFINITY ? 0.f : -m_ref, tSj, se, sr);
-            l += se;
-            l_rounded += sr;
+                l += se;
+                l_rounded += sr;
+            } else {
+                const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+                float se;
+                exp_pack_store<BC>(s, c2, neg_m, tSj, se);
+                l += se;
+                if (m_tile != -INFINITY) l_rounded += max_weight_rounding(mx, c2, neg_m);
+            }
             // single-tile items: S(j) ready no longer implies P(j-1) V done;
             // wait for it before O may be rescaled (it is normally done by now)
             if (single && j > item.kv0) {
@@ -883,6 +897,7 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
         o_phase ^= 1u;
         ptx::tc_fence_after_sync();
         // a row that saw no key at all (possible only with the paged cache) is empty: O = 0, LSE = -inf
+        if constexpr (!F8) l_rounded += l;
         float inv_l = l_rounded > 0.f ? 1.f / l_rounded : 0.f;
         if constexpr (F8) inv_l *= out_scale;
         const bool live = qg < p.Nq;
