@@ -17,8 +17,10 @@ fa_fwd_paged or fa_fwd_fp8 on the same workload instead.
 * roofline: the kernel's average launch time (CUDA events on its stream)
   against the measured dense-bf16 peak; traffic from the committed ncu
   summary when the kernel source still matches it.
-* cpu_baseline: the fp64 oracle on a bounded sample of rows, host cores.
-* --impl reference: the oracle alone, timed per step on a bounded sample.
+* cpu_baseline: the fp64 oracle on the host cores, wall clock: a full run of
+  the workload when it fits the --cpu-seconds budget, else a row sample.
+* --impl reference: the oracle alone, each timed step a full run of the
+  workload when all steps fit in about four minutes, else a row sample.
 Under torchrun (N > 1) every rank runs its own batch (weak scaling, no
 collective on the data path); rank 0 prints the max-over-ranks result.
 """
@@ -138,67 +140,130 @@ def measured_peaks():
 
 # ------------------------------------------------------------------ clocks
 
+# Polls NVML in a child process (so the benchmark's own thread never waits for
+# the interpreter lock): prints "time sm_mhz max_mhz reason_bits" every period.
+# Read-only NVML queries; nothing is set.
+_NVML_POLLER = r"""
+import ctypes, sys, time
+bus, index, period = sys.argv[1].encode(), int(sys.argv[2]), float(sys.argv[3])
+lib = ctypes.CDLL("libnvidia-ml.so.1")
+if lib.nvmlInit_v2() != 0:
+    sys.exit(2)
+h = ctypes.c_void_p()
+if not bus or lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0:
+    if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h)) != 0:
+        sys.exit(3)
+reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or lib.nvmlDeviceGetCurrentClocksThrottleReasons
+mx, mhz, bits = ctypes.c_uint(0), ctypes.c_uint(0), ctypes.c_ulonglong(0)
+lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+print("ready", flush=True)
+while True:
+    if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0 and reasons(h, ctypes.byref(bits)) == 0:
+        sys.stdout.write(f"{time.time():.6f} {mhz.value} {mx.value} {bits.value}\n")
+        sys.stdout.flush()
+    time.sleep(period)
+"""
+
+
 class ClockSampler:
-    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons."""
+    """SM clock and clock-event (throttle) reasons of the benchmarked GPU during
+    the timed region: NVML polled every `period` seconds by a child process,
+    or nvidia-smi every 100 ms where NVML cannot be loaded."""
 
-    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index: int):
-        self.samples = []
+    def __init__(self, torch_index: int, period: float = 2.5e-4):
+        self.samples = []          # (time, sm_mhz, max_mhz, reason bits)
+        self.period = period
+        self.source = "nvml"
         self.proc = None
+        bus = ""
+        try:   # the CUDA device's PCI address (NVML may number the GPUs differently)
+            import torch
+            pr = torch.cuda.get_device_properties(torch_index)
+            bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+        except Exception:   # noqa: BLE001 -- older torch without the PCI fields
+            bus = ""
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.proc = subprocess.Popen([sys.executable, "-c", _NVML_POLLER, bus, str(torch_index), str(period)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            ready = self.proc.stdout.readline().strip() == "ready"
         except OSError:
+            ready = False
+        if not ready:
+            self._kill()
+            self.source = "nvidia-smi"
+            self.period = 0.1
+            self._start_smi(torch_index)
             return
-        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread = threading.Thread(target=self._read_nvml, daemon=True)
         self.thread.start()
 
-    def _read(self):
+    def _read_nvml(self):
         for line in self.proc.stdout:
-            self.samples.append((time.time(), line.strip()))
+            parts = line.split()
+            try:
+                self.samples.append((float(parts[0]), float(parts[1]), float(parts[2]), int(parts[3])))
+            except (IndexError, ValueError):
+                continue
 
-    def stop(self):
+    def _start_smi(self, gpu_index):
+        fields = ("timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={fields}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read_smi, daemon=True)
+        self.thread.start()
+
+    def _read_smi(self):
+        bitmap = {4: 0x8, 5: 0x40, 6: 0x20, 7: 0x4}
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            try:
+                bits = sum(b for i, b in bitmap.items() if parts[i].lower() == "active")
+                self.samples.append((time.time(), float(parts[1]), float(parts[2]), bits))
+            except (IndexError, ValueError):
+                continue
+
+    def _kill(self):
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+            self.proc = None
+
+    def stop(self):
+        self._kill()
 
     def summary(self, t0, t1):
-        rows = []
-        for ts, line in self.samples:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:8]))
-            except ValueError:
-                continue
-        inside = [r for r in rows if t0 <= r[0] <= t1]
+        inside = [r for r in self.samples if t0 <= r[0] <= t1]
         window = "timed region"
         if len(inside) < 3:   # very short timed region: take the samples nearest to it
-            inside = sorted(rows, key=lambda r: abs(r[0] - 0.5 * (t0 + t1)))[:5]
+            inside = sorted(self.samples, key=lambda r: abs(r[0] - 0.5 * (t0 + t1)))[:5]
             window = "nearest samples (timed region shorter than the sampling period)"
         if not inside:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock samples"], "source": self.source}
+        reasons = sorted({name for r in inside for bit, name in self.REASONS.items() if r[3] & bit})
         return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
-                "reasons": reasons, "samples": len(inside), "window": window}
+                "reasons": reasons, "samples": len(inside), "window": window, "source": self.source,
+                "period_ms": round(self.period * 1e3, 3)}
 
 
 # ---------------------------------------------------------------- CPU legs
 
-def oracle_sample(w, q, k, v, target_s, nthreads):
-    """Time the oracle on a bounded row sample sized to ~target_s seconds.
-
-    Returns (TFLOPS, seconds, rows, threads)."""
+def oracle_time(w, q, k, v, budget_s, nthreads):
+    """Time the fp64 oracle on the workload with wall-clock time: one full run
+    when a probe of 64 random rows predicts that it ends within budget_s, else
+    a random row sample sized to about budget_s.
+    Returns (TFLOPS, seconds, rows, threads, full_run)."""
     import oracle
     rng = np.random.default_rng(0)
     per_row = lambda rows: sum(4 * (min(w.Nk, (r % w.Nq) + 1) if w.causal else w.Nk) * w.d for r in rows)
@@ -206,38 +271,54 @@ def oracle_sample(w, q, k, v, target_s, nthreads):
     t = time.perf_counter()
     oracle.attention_rows(q, k, v, w.scale, w.causal, rows=probe, nthreads=nthreads)
     dt = max(time.perf_counter() - t, 1e-4)
-    n = int(min(w.B * w.H * w.Nq, max(64, 64 * target_s / dt)))
+    rate = per_row(probe) / dt                      # FLOP/s of the oracle on these cores
+    if w.flops / rate <= budget_s:
+        t = time.perf_counter()
+        oracle.attention(q, k, v, w.scale, w.causal, nthreads=nthreads)
+        dt = time.perf_counter() - t
+        return w.flops / dt / 1e12, dt, w.B * w.H * w.Nq, nthreads, True
+    n = int(min(w.B * w.H * w.Nq, max(64, 64 * budget_s / dt)))
     rows = rng.integers(0, w.B * w.H * w.Nq, n)
     t = time.perf_counter()
     oracle.attention_rows(q, k, v, w.scale, w.causal, rows=rows, nthreads=nthreads)
     dt = time.perf_counter() - t
-    return per_row(rows) / dt / 1e12, dt, n, nthreads
+    return per_row(rows) / dt / 1e12, dt, n, nthreads, False
+
+
+def oracle_note(rows, dt, threads, full):
+    what = f"full run of the workload ({rows} query rows)" if full else f"{rows} random query rows of the workload"
+    return f"{what}, fp64 three-pass oracle, {dt:.1f} s wall clock, {threads} threads"
 
 
 def run_reference(args, w):
+    """The oracle as the reference arm: warm-up steps run short row samples,
+    each timed step a full run of the workload when all of them fit in about
+    four minutes, else a row sample per step sized to fit."""
     rank = env_int("RANK", 0)
     if rank != 0:
         return 0
     q, k, v, _ = inputs.make_inputs(w)
     cores = os.cpu_count() or 1
-    per_step = min(5.0, max(0.5, 120.0 / max(1, args.steps + args.warmup)))
+    per_step = max(0.5, 240.0 / max(1, args.steps))
     for _ in range(args.warmup):
-        oracle_sample(w, q, k, v, per_step, cores)
-    vals, secs, nrows = [], 0.0, 0
+        oracle_time(w, q, k, v, 0.0, cores)          # a short sample: threads and caches warm
+    vals, secs, nrows, fulls = [], 0.0, 0, []
     for _ in range(args.steps):
-        tf, dt, n, _ = oracle_sample(w, q, k, v, per_step, cores)
+        tf, dt, n, _, full = oracle_time(w, q, k, v, per_step, cores)
         vals.append(tf)
         secs += dt
         nrows += n
+        fulls.append(full)
     value = statistics.median(vals)
+    note = (f"{args.steps} full runs of the workload" if all(fulls) else
+            f"{nrows} random query rows over {args.steps} steps (a full run would exceed the time budget)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(w, None),
         "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
-                         "sample": f"{nrows} rows over {args.steps} steps, fp64 three-pass oracle, "
-                                   f"{cores} threads"},
+                         "sample": f"{note}, fp64 three-pass oracle, wall clock, {cores} threads"},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -456,10 +537,9 @@ def run_ours(args, w):
             "clocks": sampler.summary(t0, t1) if sampler else None,
         }
         if world == 1 and not args.no_cpu_baseline:
-            tf, dt, n, cores = oracle_sample(w, q, k, v, args.cpu_seconds, os.cpu_count() or 1)
+            tf, dt, n, cores, full = oracle_time(w, q, k, v, args.cpu_seconds, os.cpu_count() or 1)
             line["cpu_baseline"] = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
-                                    "sample": f"{n} random query rows of the workload, fp64 three-pass "
-                                              f"oracle, {dt:.1f} s"}
+                                    "sample": oracle_note(n, dt, cores, full)}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -473,7 +553,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=30.0,
+                    help="time budget of the oracle leg: a full run of the workload if it fits, else a row sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     ap.add_argument("--block-size", type=int, default=64, help="page size of --path paged")

@@ -190,9 +190,27 @@ __host__ __device__ __forceinline__ Item decode_item(const FwdParams &p, int w, 
         r = w / p.kv_splits; split = w - r * p.kv_splits; first = 0; single = 0;
     } else if (w < p.n_pair_items) {
         r = w; first = 0; single = 0;
-    } else {
-        const int s = w - p.n_pair_items;
+    } else if (!p.causal) {
+        const int s = w - p.n_pair_items;   // all tiles cost the same: both tiles of a pair in turn
         r = p.n_pair_items + (s >> 1); first = s & 1; single = 1;
+    } else {
+        // causal: singles by decreasing cost, i.e. per pair index (heads in
+        // chunks of BH) first the upper tile 2p+1 of every head, then the
+        // lower tile 2p, so the snake's second round pairs heavy with light
+        const int s = w - p.n_pair_items;
+        const int r0 = p.n_pair_items;
+        // split pairs in the first, partial chunk (the split pairs run to the
+        // end of the list, which is a whole number of chunks)
+        const int m0 = (p.BH - r0 % p.BH) % p.BH;
+        if (s < 2 * m0) {
+            first = s < m0 ? 1 : 0;
+            r = r0 + (s < m0 ? s : s - m0);
+        } else {
+            const int s2 = s - 2 * m0, c = s2 / (2 * p.BH), rem = s2 - c * 2 * p.BH;
+            first = rem < p.BH ? 1 : 0;
+            r = r0 + m0 + c * p.BH + (rem < p.BH ? rem : rem - p.BH);
+        }
+        single = 1;
     }
     const int per_group = p.heads_per_group * p.P;
     const int g = r / per_group;

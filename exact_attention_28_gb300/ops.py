@@ -321,8 +321,20 @@ def fa_fwd_splitkv(q, k, v, o=None, lse=None, scale=None, causal=False, num_spli
 
 def fa_fwd_splitkv_noalloc(q, k, v, o, lse, scale=None, causal=False, num_splits=0, stream=None):
     """Split-key forward whose partials live in the library's fixed scratch area
-    (no allocation anywhere on this call; o and lse are caller-provided)."""
+    (no allocation anywhere on this call; o and lse are caller-provided:
+    o bf16 like q, lse fp32 [B, H, Nq], both contiguous on q's device)."""
+    for t in (q, k, v):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()):
+            raise TypeError("q, k, v must be contiguous bf16 CUDA tensors")
     B, H, Nq, Nk, d = _shape(q, k)
+    if k.shape != (B, H, Nk, d) or v.shape != (B, H, Nk, d):
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)} k {tuple(k.shape)} v {tuple(v.shape)}")
+    if not (isinstance(o, torch.Tensor) and o.dtype == torch.bfloat16 and o.shape == q.shape
+            and o.is_contiguous() and o.device == q.device):
+        raise TypeError("o must be a contiguous bf16 tensor shaped like q on q's device")
+    if not (isinstance(lse, torch.Tensor) and lse.dtype == torch.float32 and lse.shape == (B, H, Nq)
+            and lse.is_contiguous() and lse.device == q.device):
+        raise TypeError("lse must be a contiguous fp32 tensor [B, H, Nq] on q's device")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     _check(load_library().fa_fwd_splitkv_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),

@@ -123,6 +123,16 @@ fa_status fa_fwd_test_missing_load(const void *Q, const void *K, const void *V, 
  * bounded waits expires.  Returns FA_OK, FA_ERR_TIMEOUT, or FA_ERR_CUDA if the
  * synchronisation itself failed or a backward kernel was given a shared-memory
  * base it could not align (it then computes nothing).
+ *
+ * Scope: there is one status word per device per process, shared by every
+ * stream and every host thread that runs this library's kernels on that
+ * device.  A timeout in any of them is reported to the first caller that
+ * checks after it (whatever stream that caller names; only that stream is
+ * synchronised, so a kernel still running elsewhere may set the word after
+ * the check) and the check clears it for everyone.  A caller that runs
+ * several streams or threads and must know which call failed should check
+ * after each call with the other streams idle, or treat FA_ERR_TIMEOUT as
+ * "some call since the last check on this device failed".
  */
 fa_status fa_check_device_status(fa_stream_t stream);
 
@@ -333,7 +343,9 @@ fa_status fa_fwd_splitkv_noalloc(const void *Q, const void *K, const void *V, vo
  * one (batch*head, pair of 128-row query tiles) or a single tile, over all
  * the key/value tiles it can see or one slice of them -- the parallelisation
  * over batch x heads x query blocks that "9.4 FlashAttention 与 FlashMLA"
- * section 9.4.4 describes for FA2.
+ * section 9.4.4 describes for FA2.  Key/value tiles hold 128 keys at d = 128
+ * and 64 keys at d = 64, where two CTAs run on each SM (up to 2 * num_sms
+ * CTAs).
  *
  *   items     int32 [capacity][8], caller-owned, may be NULL to only count:
  *             {cta, round, batch*head, first query row, first KV tile,

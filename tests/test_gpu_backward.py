@@ -103,3 +103,63 @@ def test_autograd_wrapper_matches_the_oracle(ops):
     check("dQ", Q.grad, rQ)
     check("dK", K.grad, rK)
     check("dV", V.grad, rV)
+
+
+def elementwise_bounds(q, k, v, do, scale, causal):
+    """Per-element error bounds of dQ, dK, dV from the arithmetic, in fp64.
+
+    The kernels round P and dS = P (dP - D) to bf16 (relative error <= 2^-9)
+    before the gradient GEMMs, accumulate in fp32 and round the result to
+    bf16 (<= 2^-9 of the element).  So element (i, c) of dQ = scale dS K is
+    off by at most 2^-9 |dQ_ic| + 2^-9 scale sum_j |dS_ij| |K_jc| plus fp32
+    accumulation error, and dK, dV likewise with dS^T Q and P^T dO.  D =
+    rowsum(dO * O) is formed from the forward's bf16 O (relative error about
+    2^-9 per element), so dS_ij also carries -P_ij dD_i with |dD_i| <= 2^-9
+    sum_c |dO_ic| |O_ic|: on rows whose exact dS vanishes (a query that sees
+    one key) this is the whole gradient.  The bounds below take twice those
+    factors (2^-8), which also covers the recomputation of P from the stored
+    LSE in fp32.
+    """
+    f = oracle.bf16_bits_to_f64
+    Q, K, V, dO = f(q), f(k), f(v), f(do)
+    B, H, Nq, d = Q.shape
+    Nk = K.shape[2]
+    vis = np.ones((Nq, Nk), dtype=bool) if not causal else (np.arange(Nk)[None, :] <= np.arange(Nq)[:, None])
+    bounds = [np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)]
+    for b in range(B):
+        for h in range(H):
+            S = np.where(vis, scale * (Q[b, h] @ K[b, h].T), -np.inf)
+            P = np.exp(S - S.max(axis=1, keepdims=True))
+            P /= P.sum(axis=1, keepdims=True)
+            O = P @ V[b, h]
+            dS = P * (dO[b, h] @ V[b, h].T - (dO[b, h] * O).sum(axis=1, keepdims=True))
+            dD = 2.0 ** -8 * (np.abs(dO[b, h]) * np.abs(O)).sum(axis=1)     # error of D from the bf16 O
+            bounds[0][b, h] = 2.0 ** -8 * abs(scale) * (np.abs(dS) @ np.abs(K[b, h])) + \
+                abs(scale) * dD[:, None] * (P @ np.abs(K[b, h]))
+            bounds[1][b, h] = 2.0 ** -8 * abs(scale) * (np.abs(dS).T @ np.abs(Q[b, h])) + \
+                abs(scale) * (P.T @ (dD[:, None] * np.abs(Q[b, h])))
+            bounds[2][b, h] = 2.0 ** -8 * (P.T @ np.abs(dO[b, h]))
+    return bounds
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq,Nk", [(128, 128), (200, 300), (257, 129)])
+def test_backward_every_element_within_its_bound(ops, d, causal, Nq, Nk):
+    # element-wise: |G_gpu - G_ref| <= 2^-8 |G_ref| + (bf16 rounding of the
+    # summed terms, see elementwise_bounds) + 1e-6, on every entry
+    q, k, v = inputs.custom_inputs(4321 + Nq, 1, 2, Nq, Nk, d)
+    do = inputs.normal_bf16(77 + Nk, (1, 2, Nq, d))
+    scale = float(np.float32(1 / math.sqrt(d)))
+    Q, K, V, dO = to_dev(q), to_dev(k), to_dev(v), to_dev(do)
+    O, L = ops.fa_fwd(Q, K, V, scale=scale, causal=causal)
+    grads = ops.fa_bwd(Q, K, V, O, L, dO, scale=scale, causal=causal)
+    ops.check_device_status()
+    f = oracle.bf16_bits_to_f64
+    refs = backward.backward_heads(f(q), f(k), f(v), f(do), scale, causal)
+    for name, g, r, extra in zip(("dQ", "dK", "dV"), grads, refs, elementwise_bounds(q, k, v, do, scale, causal)):
+        err = np.abs(g.float().cpu().numpy().astype(np.float64) - r)
+        bound = 2.0 ** -8 * np.abs(r) + extra + 1e-6
+        worst = np.unravel_index(np.argmax(err / bound), err.shape)
+        assert np.all(err <= bound), (f"{name}: element {worst} error {err[worst]:.3e} > bound {bound[worst]:.3e} "
+                                      f"(ref {r[worst]:.3e})")
