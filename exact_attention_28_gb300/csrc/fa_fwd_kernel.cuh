@@ -457,6 +457,78 @@ __device__ void producer_role(const FwdParams &p, const Shared &sh, uint32_t sme
     }
 }
 
+// Paged cache: the whole producer warp runs this loop.  Lane 0 waits for free
+// ring slots and arms the barriers; lane c + chunks * s copies box s (keys
+// s * rows .. of the tile, one page) of column chunk c, so the up to 16 boxes
+// of a tile of 16-key pages leave in one warp instruction instead of one
+// after another, and each lane looks up the page of its own box, one tile
+// ahead.
+template <int D, int MODE>
+__device__ void producer_role_paged(const FwdParams &p, const Shared &sh, uint32_t smem_q, uint32_t smem_ring,
+                                    uint32_t &loads_issued, uint32_t &q_arms, int lane) {
+    using C = Config<D, false>;
+    const uint64_t pol_q = ptx::l2_policy_evict_first();
+    const uint64_t pol_kv = ptx::l2_policy_evict_last();
+    const int rows = p.block_size < C::kBC ? p.block_size : C::kBC;
+    const int copies = (C::kBC / rows) * C::kChunks;   // <= 16
+    const int box = lane / C::kChunks, chunk = lane % C::kChunks;
+    const bool mine = lane < copies;
+    uint32_t it = 0;
+    for (int k = 0;; ++k) {
+        const int w = item_of_round(p, k);
+        if (w < 0) break;
+        const Item item = resolve_item<MODE>(p, w);
+        bool ok = true;
+        if (lane == 0) {
+            if (k > 0 && !wait_bar(sh.q_empty, (k - 1) & 1, sh.abort_flag, 0, w, -1)) {
+                ok = false;
+            } else {
+                ptx::mbar_arrive_expect_tx(sh.q_full, item.ntiles * C::kQTileBytes);
+                ++q_arms;
+                for (int t = 0; t < item.ntiles; ++t)
+                    #pragma unroll
+                    for (int c = 0; c < C::kChunks; ++c)
+                        ptx::tma_load_3d(smem_q + t * C::kQTileBytes + c * C::kQChunkBytes, &p.tmQ, sh.q_full,
+                                         c * 64, item.q0 + t * kBR, item.bh, pol_q);
+            }
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        const int nkv = max(item.nk[0], item.nk[1]);
+        const int b = item.bh / p.H, h = item.bh % p.H;
+        int page_next = (mine && item.kv0 < nkv) ? page_of_box<C::kBC>(p, b, item.kv0, box, rows) : 0;
+        for (int j = item.kv0; j < nkv && ok; ++j) {
+            const int page = page_next;
+            if (mine && j + 1 < nkv) page_next = page_of_box<C::kBC>(p, b, j + 1, box, rows);
+            #pragma unroll 1
+            for (int which = 0; which < 2; ++which, ++it) {
+                const uint32_t slot = it % C::kSlots;
+                const uint32_t use = it / C::kSlots;
+                const uint32_t full = sh.kv_full0 + 8 * slot;
+                const bool skip = w == p.drop_load_item && j == item.kv0 && which == 0;   // test hook
+                bool armed = true;
+                if (lane == 0) {
+                    armed = wait_bar(sh.kv_empty0 + 8 * slot, (use & 1) ^ 1, sh.abort_flag, 0, w, j);
+                    if (armed && !skip) ptx::mbar_arrive_expect_tx(full, C::kKVTileBytes);
+                }
+                if (!__shfl_sync(0xffffffffu, armed, 0)) {
+                    ok = false;
+                    break;
+                }
+                __syncwarp();   // lane 0's expect_tx is ordered before the copies (the count may also go below zero)
+                if (!skip && mine) {
+                    // an unallocated page is read from block 0 (its keys are masked by the softmax)
+                    const int phy = page < 0 ? 0 : page;
+                    const int row0 = (j * C::kBC + box * rows) % p.block_size;
+                    ptx::tma_load_4d(smem_ring + slot * C::kKVTileBytes + chunk * C::kKVChunkBytes + box * rows * 128,
+                                     which ? &p.tmV : &p.tmK, full, chunk * 64, row0, h, phy, pol_kv);
+                }
+                loads_issued = it + 1;
+            }
+        }
+        if (!ok) break;
+    }
+}
+
 // ----------------------------------------------------------------- MMA warp
 
 // S_t = Q_t K_j^T: D/16 MMAs of K = 16, N = BC.  Q and K tiles are D/64
@@ -1037,8 +1109,11 @@ __global__ void __launch_bounds__(Config<D>::kThreads, Config<D>::kCtasPerSm)
         softmax_role<D, MODE>(p, sh, tmem, warp >> 2, warp & 3, lane);
     } else if (warp == kProducerWarp) {
         if constexpr (C::kRegSplit) ptx::setmaxnreg_dec<kOtherRegs>();
+        if constexpr ((MODE & kPaged) != 0)
+            producer_role_paged<D, MODE>(p, sh, smem_q, smem_ring, loads_issued, q_arms, lane);
         if (lane == 0) {
-            producer_role<D, MODE>(p, sh, smem_q, smem_ring, loads_issued, q_arms);
+            if constexpr ((MODE & kPaged) == 0)
+                producer_role<D, MODE>(p, sh, smem_q, smem_ring, loads_issued, q_arms);
             // Drain: every copy this CTA started must land before it exits.
             const uint32_t first = loads_issued > (uint32_t)C::kSlots ? loads_issued - C::kSlots : 0u;
             for (uint32_t x = first; x < loads_issued; ++x)
