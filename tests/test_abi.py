@@ -42,9 +42,38 @@ def test_binding_matches_header_arity(lib):
 
 
 def test_status_strings(lib):
-    for s in range(6):
+    for s in range(7):
         assert ops.status_string(s)
     assert "unknown" in ops.status_string(99)
+
+
+def test_status_mapping_to_python_errors(lib):
+    """Each status code has its own name in the header's enum order, and the
+    binding turns every non-OK status into an FAError carrying that code."""
+    names = ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED", "FA_ERR_CUDA",
+             "FA_ERR_TIMEOUT", "FA_ERR_TOO_LARGE"]
+    assert [getattr(ops, n) for n in names] == list(range(7))
+    for code, name in enumerate(names):
+        assert ops.status_string(code).startswith(name)
+        if code == ops.FA_OK:
+            ops._check(code)   # no exception
+            continue
+        with pytest.raises(ops.FAError) as err:
+            ops._check(code)
+        assert err.value.status == code and name in str(err.value)
+    assert "wait expired" in ops.status_string(ops.FA_ERR_TIMEOUT)
+
+
+def test_device_status_check_without_a_gpu_is_an_error(lib):
+    # the status word lives on the device: without one the check cannot
+    # report FA_OK (it would hide a failure), it reports FA_ERR_CUDA
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert lib.fa_check_device_status(None) == ops.FA_ERR_CUDA
+    with pytest.raises(ops.FAError) as err:
+        ops.check_device_status(0)
+    assert err.value.status == ops.FA_ERR_CUDA
 
 
 GOOD = dict(q=0x10000, k=0x20000, v=0x30000, o=0x40000, lse=0x50000,
