@@ -906,16 +906,30 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
                 s_phase ^= 1u;
             }
             ptx::tc_fence_after_sync();
+            // S; at head dimension 64 the load's own max reduction gives the row
+            // maximum for a positive scale (a negative scale needs the minimum:
+            // software).  At 128 it measured no faster than the software maximum.
+            constexpr bool kHwMax = BC == 64;
             uint32_t s[BC];
-            if constexpr (BC == 128)
-                ptx::tmem_load_128cols(tSj, s);
-            else
-                ptx::tmem_load_64cols(tSj, s);
+            float mparts[BC / 32];
+            if (kHwMax && pos) {
+                if constexpr (BC == 128)
+                    ptx::tmem_load_128cols_max(tSj, s, mparts);
+                else
+                    ptx::tmem_load_64cols_max(tSj, s, mparts);
+            } else {
+                if constexpr (BC == 128)
+                    ptx::tmem_load_128cols(tSj, s);
+                else
+                    ptx::tmem_load_64cols(tSj, s);
+            }
             const int kvalid = key_lim - j * BC;
+            bool masked;   // warp-uniform: some key of this tile is invisible to some row of the warp
             if constexpr ((MODE & kPaged) != 0) {
                 // bit s: box s lies in an unallocated page (warp-uniform)
                 const uint32_t holes = __ballot_sync(0xffffffffu, box_page < 0);
-                if (__any_sync(0xffffffffu, kvalid < BC) || holes) {   // warp-uniform masked path
+                masked = __any_sync(0xffffffffu, kvalid < BC) || holes;
+                if (masked) {
                     // column mask, bit c % 32 of word c / 32 (a box holds >= 16 columns)
                     uint32_t cm[BC / 32];
                     #pragma unroll
@@ -928,13 +942,22 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
                         if (c >= kvalid || ((cm[c >> 5] >> (c & 31)) & 1u)) s[c] = __float_as_uint(mask_val);
                 }
             } else {
-                if (__any_sync(0xffffffffu, kvalid < BC)) {   // warp-uniform masked path
+                masked = __any_sync(0xffffffffu, kvalid < BC);
+                if (masked) {
                     #pragma unroll
                     for (int c = 0; c < BC; ++c)
                         if (c >= kvalid) s[c] = __float_as_uint(mask_val);
                 }
             }
-            const float mx = row_extreme<BC>(s, pos);
+            float mx;
+            if (kHwMax && pos && !masked) {
+                if constexpr (BC == 128)
+                    mx = fmaxf(ptx::max3(mparts[0], mparts[1], mparts[2]), mparts[3]);
+                else
+                    mx = fmaxf(mparts[0], mparts[1]);
+            } else {
+                mx = row_extreme<BC>(s, pos);   // over the masked scores
+            }
             const float m_tile = kvalid > 0 ? mx * c2 : -INFINITY;
             float alpha = 1.f;
             if (m_tile > m_ref + (F8 ? kTauF8 : kTau)) {
