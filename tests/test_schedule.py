@@ -107,6 +107,21 @@ def test_causal_load_balance():
     assert load.max() / load.mean() < 1.10
 
 
+def test_causal_single_tiles_pair_heavy_with_light():
+    # 4 x 16 x 1024 causal at d = 64: 512 single-tile items (64-key tiles, 2 to
+    # 16 key steps each) on 304 CTAs.  Listing each pair index's upper tiles
+    # first makes the snake's second round give the lightest items to the CTAs
+    # with the heaviest first items: at most 16 key steps per CTA (the optimum:
+    # the heaviest item alone has 16; the mean is 15.2).
+    items = ops.schedule(4, 16, 1024, 1024, 64, True, 152)
+    assert np.all(items[:, 6] == -1)                       # all single-tile items
+    load = cta_loads(items, key=lambda nk: nk)
+    assert len(load) == 304 and load.max() == 16
+    # the work list is heaviest first inside each round's snake
+    first_round = items[items[:, 1] == 0]
+    assert (first_round[:, 5] - first_round[:, 4]).max() == 16
+
+
 def test_schedule_argument_errors():
     n = ops.ctypes.c_int64(0)
     lib = ops.load_library()
