@@ -168,6 +168,18 @@ int setup_params(fa::FwdParams &p, int B, int H, int Nq, int Nk, int d, float sc
     p.heads_per_group = heads_per_group(BH, Nk, d, causal);
     p.kv_splits = kv_splits > 1 ? kv_splits : 1;
     p.drop_load_item = -1;
+    // the decode's invariant divisors (all >= 1; every dividend is < 2^31)
+    const int64_t groups = (BH + p.heads_per_group - 1) / p.heads_per_group;
+    p.fd_splits = fa::make_fastdiv(static_cast<uint32_t>(p.kv_splits));
+    p.fd_per_group = fa::make_fastdiv(static_cast<uint32_t>(p.heads_per_group) * static_cast<uint32_t>(p.P));
+    p.fd_hg = fa::make_fastdiv(static_cast<uint32_t>(p.heads_per_group));
+    p.fd_last_gsize = fa::make_fastdiv(static_cast<uint32_t>(BH - (groups - 1) * p.heads_per_group));
+    p.fd_bh = fa::make_fastdiv(static_cast<uint32_t>(BH));
+    p.fd_2bh = fa::make_fastdiv(static_cast<uint32_t>(2 * BH));
+    p.H = H;
+    p.fd_h = fa::make_fastdiv(static_cast<uint32_t>(H));
+    p.bc_shift = p.bc == 64 ? 6 : 7;
+    p.block_shift = 0;
     if (p.kv_splits > 1) {
         const int64_t NP = static_cast<int64_t>(p.BH) * p.P;
         p.n_pair_items = static_cast<int>(NP);
@@ -354,6 +366,7 @@ fa_status run_paged(const void *Q, const void *K_cache, const void *V_cache, con
     p.LSE_part = LSE_part;
     p.H = H;
     p.block_size = block_size;
+    p.block_shift = 31 - __builtin_clz(static_cast<unsigned>(block_size));   // a power of two, 16..256
     p.max_blocks = max_blocks;
     p.block_table = block_table;
     p.seq_lens = seq_lens;

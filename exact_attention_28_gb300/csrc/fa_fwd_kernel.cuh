@@ -132,6 +132,32 @@ struct Config {
 // Keys per K/V tile for head dimension d (the host's view of Config::kBC).
 __host__ __device__ constexpr int kv_tile_keys(int d) { return d == 64 ? Config<64>::kBC : Config<128>::kBC; }
 
+// Division of a 32-bit unsigned integer by an invariant divisor d >= 1 by a
+// multiplication (Granlund and Montgomery, "Division by invariant integers
+// using multiplication", PLDI 1994, section 4): with l = ceil(log2 d),
+// m = floor(2^32 (2^l - d) / d) + 1 and t = floor(m n / 2^32),
+// n / d = (t + ((n - t) >> min(l, 1))) >> max(l - 1, 0), exact for every n.
+// The work-item decode divides by the head count, the heads per group and
+// the key slices; hardware integer division by a runtime value takes tens of
+// dependent instructions, which every role paid at every item.
+struct FastDiv {
+    uint32_t d, m, sh1, sh2;
+};
+__host__ inline FastDiv make_fastdiv(uint32_t d) {
+    uint32_t l = 0;
+    while ((uint64_t{1} << l) < d) ++l;   // d < 2^31 here, so l <= 31 and nothing overflows
+    const uint64_t m = ((uint64_t{1} << 32) * ((uint64_t{1} << l) - d)) / d + 1;
+    return FastDiv{d, static_cast<uint32_t>(m), l < 1 ? l : 1u, l > 1 ? l - 1 : 0u};
+}
+__host__ __device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f) {
+#ifdef __CUDA_ARCH__
+    const uint32_t t = __umulhi(f.m, n);
+#else
+    const uint32_t t = static_cast<uint32_t>((static_cast<uint64_t>(f.m) * n) >> 32);
+#endif
+    return (t + ((n - t) >> f.sh1)) >> f.sh2;
+}
+
 struct FwdParams {
     CUtensorMap tmQ;   // [BH][Nq][D] bf16, box {64, 128, 1}, 128-byte swizzle
     CUtensorMap tmK;   // [BH][Nk][D]
@@ -163,6 +189,10 @@ struct FwdParams {
     // test hook (fa_fwd_test_missing_load): the first K tile of this work
     // item is never loaded, so a bounded wait expires; -1 in every other call
     int drop_load_item;
+    // invariant divisors of the work-item decode (set with the sizes above)
+    FastDiv fd_splits, fd_per_group, fd_hg, fd_last_gsize, fd_bh, fd_2bh, fd_h;
+    int bc_shift;          // log2(bc)
+    int block_shift;       // paged: log2(block_size)
 };
 
 struct Item {
@@ -187,7 +217,7 @@ struct Item {
 __host__ __device__ __forceinline__ Item decode_item(const FwdParams &p, int w, bool splitting) {
     int r, first, single, split = 0;
     if (splitting) {
-        r = w / p.kv_splits; split = w - r * p.kv_splits; first = 0; single = 0;
+        r = static_cast<int>(fdiv(w, p.fd_splits)); split = w - r * p.kv_splits; first = 0; single = 0;
     } else if (w < p.n_pair_items) {
         r = w; first = 0; single = 0;
     } else if (!p.causal) {
@@ -201,25 +231,28 @@ __host__ __device__ __forceinline__ Item decode_item(const FwdParams &p, int w, 
         const int r0 = p.n_pair_items;
         // split pairs in the first, partial chunk (the split pairs run to the
         // end of the list, which is a whole number of chunks)
-        const int m0 = (p.BH - r0 % p.BH) % p.BH;
+        const int r0_mod = r0 - static_cast<int>(fdiv(r0, p.fd_bh)) * p.BH;
+        const int m0 = r0_mod ? p.BH - r0_mod : 0;
         if (s < 2 * m0) {
             first = s < m0 ? 1 : 0;
             r = r0 + (s < m0 ? s : s - m0);
         } else {
-            const int s2 = s - 2 * m0, c = s2 / (2 * p.BH), rem = s2 - c * 2 * p.BH;
+            const int s2 = s - 2 * m0, c = static_cast<int>(fdiv(s2, p.fd_2bh)), rem = s2 - c * 2 * p.BH;
             first = rem < p.BH ? 1 : 0;
             r = r0 + m0 + c * p.BH + (rem < p.BH ? rem : rem - p.BH);
         }
         single = 1;
     }
     const int per_group = p.heads_per_group * p.P;
-    const int g = r / per_group;
+    const int g = static_cast<int>(fdiv(r, p.fd_per_group));
     const int rr = r - g * per_group;
     const int rest = p.BH - g * p.heads_per_group;
-    const int gsize = p.heads_per_group < rest ? p.heads_per_group : rest;
-    const int pair = p.P - 1 - rr / gsize;
+    const bool full_group = p.heads_per_group <= rest;
+    const int gsize = full_group ? p.heads_per_group : rest;
+    const int pq = static_cast<int>(fdiv(rr, full_group ? p.fd_hg : p.fd_last_gsize));
+    const int pair = p.P - 1 - pq;
     Item it;
-    it.bh = g * p.heads_per_group + rr % gsize;
+    it.bh = g * p.heads_per_group + (rr - pq * gsize);
     it.q0 = (2 * pair + first) * kBR;
     const int left = p.Tr - (2 * pair + first);
     it.ntiles = single ? 1 : (left >= 2 ? 2 : 1);
@@ -232,7 +265,7 @@ __host__ __device__ __forceinline__ Item decode_item(const FwdParams &p, int w, 
             if (p.causal) {
                 const int q_end_raw = it.q0 + (t + 1) * kBR;
                 const int q_end = q_end_raw < p.Nq ? q_end_raw : p.Nq;   // rows >= Nq are padding
-                const int need = (q_end - 1) / p.bc + 1;
+                const int need = ((q_end - 1) >> p.bc_shift) + 1;
                 nk = need < p.Tc ? need : p.Tc;
             }
         }
@@ -243,7 +276,8 @@ __host__ __device__ __forceinline__ Item decode_item(const FwdParams &p, int w, 
     it.q_shift = 0;
     if (splitting) {
         const int nkv = vis[0] > vis[1] ? vis[0] : vis[1];
-        const int kb = split * nkv / p.kv_splits, ke = (split + 1) * nkv / p.kv_splits;
+        const int kb = static_cast<int>(fdiv(split * nkv, p.fd_splits));
+        const int ke = static_cast<int>(fdiv((split + 1) * nkv, p.fd_splits));
         it.kv0 = kb;
         #pragma unroll
         for (int t = 0; t < 2; ++t) it.nk[t] = vis[t] < ke ? vis[t] : ke;
@@ -268,7 +302,7 @@ __device__ __forceinline__ Item resolve_item(const FwdParams &p, int w) {
         return it;
     } else {
         const int cap = p.max_blocks * p.block_size;
-        int seq = __ldg(p.seq_lens + it.bh / p.H);
+        int seq = __ldg(p.seq_lens + fdiv(it.bh, p.fd_h));
         seq = seq < 0 ? 0 : (seq > cap ? cap : seq);
         it.seq_len = seq;
         it.q_shift = seq - p.Nq;
@@ -280,11 +314,12 @@ __device__ __forceinline__ Item resolve_item(const FwdParams &p, int w) {
                 const int q_end = min(p.Nq, it.q0 + (t + 1) * kBR);
                 keys = min(seq, q_end + it.q_shift);
             }
-            vis[t] = keys > 0 ? (keys + p.bc - 1) / p.bc : 0;
+            vis[t] = keys > 0 ? ((keys + p.bc - 1) >> p.bc_shift) : 0;
         }
         if constexpr ((MODE & kSplit) != 0) {
             const int nkv = max(vis[0], vis[1]);
-            const int kb = it.split * nkv / p.kv_splits, ke = (it.split + 1) * nkv / p.kv_splits;
+            const int kb = static_cast<int>(fdiv(it.split * nkv, p.fd_splits));
+            const int ke = static_cast<int>(fdiv((it.split + 1) * nkv, p.fd_splits));
             it.kv0 = kb;
             #pragma unroll
             for (int t = 0; t < 2; ++t) it.nk[t] = min(vis[t], ke);
@@ -303,7 +338,7 @@ __device__ __forceinline__ Item resolve_item(const FwdParams &p, int w) {
 // table (keys past the table lie beyond the sequence and are masked anyway).
 template <int BC>
 __device__ __forceinline__ int page_of_box(const FwdParams &p, int b, int j, int s, int rows) {
-    const int lp = (j * BC + s * rows) / p.block_size;
+    const int lp = (j * BC + s * rows) >> p.block_shift;
     return lp < p.max_blocks ? __ldg(p.block_table + static_cast<size_t>(b) * p.max_blocks + lp) : -1;
 }
 
@@ -325,7 +360,7 @@ __device__ __forceinline__ void tma_load_paged_tile(const FwdParams &p, const CU
     for (int s = 0; s < 8; ++s) {
         if (s * rows >= BC) break;
         const int phy = pg[s] < 0 ? 0 : pg[s];
-        const int row0 = (j * BC + s * rows) % p.block_size;
+        const int row0 = (j * BC + s * rows) & (p.block_size - 1);
         for (int c = 0; c < chunks; ++c)
             ptx::tma_load_4d(dst + c * BC * 128 + s * rows * 128, map, bar, c * 64, row0, h, phy, pol);
     }
@@ -417,13 +452,13 @@ __device__ void producer_role(const FwdParams &p, const Shared &sh, uint32_t sme
         [[maybe_unused]] int pg[8], pg_next[8];
         [[maybe_unused]] const int rows = p.block_size < C::kBC ? p.block_size : C::kBC;
         if constexpr ((MODE & kPaged) != 0)
-            if (item.kv0 < nkv) pages_of_tile<C::kBC>(p, item.bh / p.H, item.kv0, rows, pg_next);
+            if (item.kv0 < nkv) pages_of_tile<C::kBC>(p, fdiv(item.bh, p.fd_h), item.kv0, rows, pg_next);
         bool ok = true;
         for (int j = item.kv0; j < nkv && ok; ++j) {
             if constexpr ((MODE & kPaged) != 0) {
                 #pragma unroll
                 for (int s = 0; s < 8; ++s) pg[s] = pg_next[s];
-                if (j + 1 < nkv) pages_of_tile<C::kBC>(p, item.bh / p.H, j + 1, rows, pg_next);
+                if (j + 1 < nkv) pages_of_tile<C::kBC>(p, fdiv(item.bh, p.fd_h), j + 1, rows, pg_next);
             }
             #pragma unroll 1
             for (int which = 0; which < 2; ++which, ++it) {
@@ -438,7 +473,8 @@ __device__ void producer_role(const FwdParams &p, const Shared &sh, uint32_t sme
                 ptx::mbar_arrive_expect_tx(full, C::kKVTileBytes);
                 const CUtensorMap *map = which ? &p.tmV : &p.tmK;
                 if constexpr ((MODE & kPaged) != 0) {
-                    tma_load_paged_tile<C::kBC>(p, map, smem_ring + slot * C::kKVTileBytes, full, item.bh % p.H, j, rows, pg,
+                    tma_load_paged_tile<C::kBC>(p, map, smem_ring + slot * C::kKVTileBytes, full,
+                                                item.bh - static_cast<int>(fdiv(item.bh, p.fd_h)) * p.H, j, rows, pg,
                                         C::kChunks, pol_kv);
                 } else if constexpr ((MODE & kFp8) != 0) {
                     // K: rows j*128.. of [Nk][128 B]; V^T: columns j*128.. of [D][ldn]
@@ -494,7 +530,7 @@ __device__ void producer_role_paged(const FwdParams &p, const Shared &sh, uint32
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         const int nkv = max(item.nk[0], item.nk[1]);
-        const int b = item.bh / p.H, h = item.bh % p.H;
+        const int b = static_cast<int>(fdiv(item.bh, p.fd_h)), h = item.bh - b * p.H;
         int page_next = (mine && item.kv0 < nkv) ? page_of_box<C::kBC>(p, b, item.kv0, box, rows) : 0;
         for (int j = item.kv0; j < nkv && ok; ++j) {
             const int page = page_next;
@@ -518,7 +554,7 @@ __device__ void producer_role_paged(const FwdParams &p, const Shared &sh, uint32
                 if (!skip && mine) {
                     // an unallocated page is read from block 0 (its keys are masked by the softmax)
                     const int phy = page < 0 ? 0 : page;
-                    const int row0 = (j * C::kBC + box * rows) % p.block_size;
+                    const int row0 = (j * C::kBC + box * rows) & (p.block_size - 1);
                     ptx::tma_load_4d(smem_ring + slot * C::kKVTileBytes + chunk * C::kKVChunkBytes + box * rows * 128,
                                      which ? &p.tmV : &p.tmK, full, chunk * 64, row0, h, phy, pol_kv);
                 }
@@ -894,7 +930,7 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
             // wait, so the load overlaps it
             [[maybe_unused]] int box_page = 0;
             if constexpr ((MODE & kPaged) != 0)
-                if (lane * page_rows < BC) box_page = page_of_box<BC>(p, item.bh / p.H, j, lane, page_rows);
+                if (lane * page_rows < BC) box_page = page_of_box<BC>(p, fdiv(item.bh, p.fd_h), j, lane, page_rows);
             // single-tile items alternate S buffers (the second is tile 1's region)
             const bool alt = single && ((j - item.kv0) & 1);
             const uint32_t tSj = tS + (alt ? static_cast<uint32_t>(BC) : 0u);
