@@ -815,6 +815,30 @@ __device__ __forceinline__ void exp_pack_store(const uint32_t (&s)[N], float c2,
     sum_exact = e0 + e1;
 }
 
+// Transpose, within each group of 8 lanes, the 8 x 8 matrix whose row j is
+// lane j's eight 16-byte pieces x[4e .. 4e+3], e = 0..7: afterwards lane j
+// holds piece j of lane e's row in x[4e .. 4e+3].  Three butterfly exchanges
+// (lane distance 4, 2, 1), each swapping the off-diagonal blocks of that size.
+__device__ __forceinline__ void transpose_8x8_pieces(uint32_t (&x)[32]) {
+    const uint32_t lane = threadIdx.x & 31u;
+    #pragma unroll
+    for (int m = 4; m >= 1; m >>= 1) {
+        const bool upper = (lane & static_cast<uint32_t>(m)) != 0;
+        #pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            if (e & m) continue;
+            #pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                // the lower lane gives away its piece e|m and takes the partner's piece e
+                const uint32_t give = upper ? x[4 * e + w] : x[4 * (e | m) + w];
+                const uint32_t take = __shfl_xor_sync(0xffffffffu, give, m);
+                if (upper) x[4 * e + w] = take;
+                else x[4 * (e | m) + w] = take;
+            }
+        }
+    }
+}
+
 // bf16(p) - p for the weight p of the tile's extreme score mx, computed with
 // the arithmetic exp_pack_store applies to that key, so the result is the
 // exact rounding error P V sees on the row's largest weight of the tile.
@@ -1070,21 +1094,27 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
             }
             if (live) p.LSE_part[prow] = lse;
         } else {
-            __nv_bfloat16 *orow = p.O + (static_cast<size_t>(item.bh) * p.Nq + qg) * D;
+            // O leaves as whole 128-byte lines: 64 columns at a time, each group of
+            // 8 lanes (8 consecutive rows) exchanges its 8 x 8 block of 16-byte
+            // pieces, so that in store e the group writes all of row e's 128 bytes.
+            const uint32_t j8 = threadIdx.x & 7u;
             #pragma unroll 1
-            for (int ch = 0; ch < D / 32; ++ch) {
-                uint32_t o[32];
-                ptx::tmem_load_32cols(tO + ch * 32, o);
-                uint32_t h[16];
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t o[64];
+                ptx::tmem_load_64cols(tO + c * 64, o);
+                uint32_t x[32];
                 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    h[i] = ptx::pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-                if (live) {
-                    // streaming stores: O is written once, keep L2 for K/V
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
-                    #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        __stcs(dst + i, make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]));
+                for (int i = 0; i < 32; ++i)
+                    x[i] = ptx::pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+                transpose_8x8_pieces(x);
+                #pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int r = qg - static_cast<int>(j8) + e;
+                    if (r < p.Nq) {
+                        // streaming stores: O is written once, keep L2 for K/V
+                        uint4 *dst = reinterpret_cast<uint4 *>(p.O + (static_cast<size_t>(item.bh) * p.Nq + r) * D + 64 * c + 8 * j8);
+                        __stcs(dst, make_uint4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]));
+                    }
                 }
             }
             if (live) p.LSE[static_cast<size_t>(item.bh) * p.Nq + qg] = lse;
