@@ -127,21 +127,32 @@ __device__ __forceinline__ void tmem_stores_then_arrive(uint32_t bar) {
     ptx::mbar_arrive(bar);
 }
 
-// Writes one TMEM row of D fp32 columns, times `mul`, as bf16 to global.
+// Writes this thread's TMEM row (row `row` of the [n_rows][D] matrix at
+// `rows`) of D fp32 columns, times `mul`, as bf16; rows >= n_rows are not
+// written.  The lanes of a warp hold consecutive rows, and each group of 8
+// lanes exchanges 16-byte pieces so that every store writes whole 128-byte
+// lines (64 columns of one row per group).
 template <int D>
-__device__ __forceinline__ void store_row_bf16(uint32_t taddr, float mul, __nv_bfloat16 *dst, bool live) {
+__device__ __forceinline__ void store_row_bf16(uint32_t taddr, float mul, __nv_bfloat16 *rows, int row, int n_rows) {
+    const uint32_t j8 = threadIdx.x & 7u;
     #pragma unroll 1
-    for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t o[32];
-        ptx::tmem_load_32cols(taddr + ch * 32, o);
-        uint32_t h[16];
+    for (int c = 0; c < D / 64; ++c) {
+        uint32_t x[32];
         #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            h[i] = ptx::pack_bf16x2(__uint_as_float(o[2 * i]) * mul, __uint_as_float(o[2 * i + 1]) * mul);
-        if (live) {
-            uint4 *p = reinterpret_cast<uint4 *>(dst + ch * 32);
+        for (int hh = 0; hh < 2; ++hh) {
+            uint32_t o[32];
+            ptx::tmem_load_32cols(taddr + c * 64 + hh * 32, o);
             #pragma unroll
-            for (int i = 0; i < 4; ++i) p[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+            for (int i = 0; i < 16; ++i)
+                x[16 * hh + i] = ptx::pack_bf16x2(__uint_as_float(o[2 * i]) * mul, __uint_as_float(o[2 * i + 1]) * mul);
+        }
+        transpose_8x8_pieces(x);
+        #pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int r = row - static_cast<int>(j8) + e;
+            if (r < n_rows)
+                *reinterpret_cast<uint4 *>(rows + static_cast<size_t>(r) * D + 64 * c + 8 * j8) =
+                    make_uint4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);
         }
     }
 }
@@ -434,9 +445,9 @@ __device__ void dkdv_elementwise_role(const BwdParams &p, const BwdShared &sh, u
     const int a_last = (n_i - 1) % kSlotsA;
     if (!wait_bar(sh.freeA0 + 8 * a_last, ((n_i - 1) / kSlotsA) & 1, sh.abort_flag, 17, blockIdx.x, n_i)) return;
     ptx::tc_fence_after_sync();
-    const bool live = key < p.Nk;
-    store_row_bf16<D>(tdV, 1.f, p.dV + out_row, live);
-    store_row_bf16<D>(tdK, p.scale, p.dK + out_row, live);
+    const size_t head = static_cast<size_t>(bh) * p.Nk * D;
+    store_row_bf16<D>(tdV, 1.f, p.dV + head, key, p.Nk);
+    store_row_bf16<D>(tdK, p.scale, p.dK + head, key, p.Nk);
 }
 
 template <int D>
@@ -578,7 +589,7 @@ __device__ void dq_elementwise_role(const BwdParams &p, const BwdShared &sh, uin
     const int a_last = (n_j - 1) % kSlotsA;
     if (!wait_bar(sh.freeA0 + 8 * a_last, ((n_j - 1) / kSlotsA) & 1, sh.abort_flag, 27, blockIdx.x, n_j)) return;
     ptx::tc_fence_after_sync();
-    store_row_bf16<D>(tdQ, p.scale, p.dQ + (static_cast<size_t>(bh) * p.Nq + q) * D, qlive);
+    store_row_bf16<D>(tdQ, p.scale, p.dQ + static_cast<size_t>(bh) * p.Nq * D, q, p.Nq);
 }
 
 template <int D>

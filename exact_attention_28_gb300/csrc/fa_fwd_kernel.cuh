@@ -1079,17 +1079,21 @@ __device__ void softmax_role(const FwdParams &p, const Shared &sh, uint32_t tmem
                                   : -INFINITY;
         if constexpr ((MODE & kSplit) != 0) {
             // partial of this key slice: O / l in fp32 and its LSE
-            float *prow_o = p.O_part + prow * D;
+            // whole 128-byte lines, as below: 32 fp32 columns are eight 16-byte pieces
+            const uint32_t j8 = threadIdx.x & 7u;
             #pragma unroll 1
             for (int ch = 0; ch < D / 32; ++ch) {
                 uint32_t o[32];
                 ptx::tmem_load_32cols(tO + ch * 32, o);
-                if (live) {
-                    float4 *dst = reinterpret_cast<float4 *>(prow_o + ch * 32);
-                    #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        __stcs(dst + i, make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
-                                                    __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l));
+                #pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * inv_l);
+                transpose_8x8_pieces(o);
+                #pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int r = qg - static_cast<int>(j8) + e;
+                    if (r < p.Nq)
+                        __stcs(reinterpret_cast<uint4 *>(p.O_part + (prow - j8 + e) * D + 32 * ch + 4 * j8),
+                               make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]));
                 }
             }
             if (live) p.LSE_part[prow] = lse;
