@@ -115,6 +115,13 @@ struct Config {
     static constexpr int kQTileBytes = kBR * D * kElem;
     static constexpr int kKVTileBytes = kBC * D * kElem;
     static constexpr int kSlots = F8 ? 10 : (D == 128 ? 5 : 8);   // K/V ring depth (tiles)
+    // Head dimension 64: K(j) and V(j) (ring indices 2i, 2i+1) share one
+    // full and one empty barrier, those of the K slot.  The MMA thread then
+    // waits once per key step instead of twice and commits one release instead
+    // of two (each costs it about as much as issuing an MMA; at d = 64 that
+    // thread paces the step).
+    static constexpr bool kPairedSlots = D == 64 && !F8;
+    static_assert(!kPairedSlots || kSlots % 2 == 0, "paired K/V slots need an even ring");
     static constexpr int kQBytes = 2 * kQTileBytes;
     static constexpr int kRingBytes = kSlots * kKVTileBytes;
     static constexpr int kBarOffset = kQBytes + kRingBytes;
@@ -460,17 +467,23 @@ __device__ void producer_role(const FwdParams &p, const Shared &sh, uint32_t sme
                 for (int s = 0; s < 8; ++s) pg[s] = pg_next[s];
                 if (j + 1 < nkv) pages_of_tile<C::kBC>(p, fdiv(item.bh, p.fd_h), j + 1, rows, pg_next);
             }
+            const bool drop = w == p.drop_load_item && j == item.kv0;   // test hook: K(j) never arrives
             #pragma unroll 1
             for (int which = 0; which < 2; ++which, ++it) {
                 const uint32_t slot = it % C::kSlots;
                 const uint32_t use = it / C::kSlots;
-                if (!wait_bar(sh.kv_empty0 + 8 * slot, (use & 1) ^ 1, sh.abort_flag, 0, w, j)) {
-                    ok = false;
-                    break;
+                // paired slots: V(j) lands on K(j)'s barrier, armed for both tiles
+                const uint32_t full = sh.kv_full0 + 8 * (C::kPairedSlots ? slot & ~1u : slot);
+                if (!C::kPairedSlots || which == 0) {
+                    if (!wait_bar(sh.kv_empty0 + 8 * slot, (use & 1) ^ 1, sh.abort_flag, 0, w, j)) {
+                        ok = false;
+                        break;
+                    }
+                    if (drop && (C::kPairedSlots || which == 0)) continue;
+                    ptx::mbar_arrive_expect_tx(full, (C::kPairedSlots ? 2 : 1) * C::kKVTileBytes);
+                } else if (drop) {
+                    continue;
                 }
-                const uint32_t full = sh.kv_full0 + 8 * slot;
-                if (w == p.drop_load_item && j == item.kv0 && which == 0) continue;   // test hook
-                ptx::mbar_arrive_expect_tx(full, C::kKVTileBytes);
                 const CUtensorMap *map = which ? &p.tmV : &p.tmK;
                 if constexpr ((MODE & kPaged) != 0) {
                     tma_load_paged_tile<C::kBC>(p, map, smem_ring + slot * C::kKVTileBytes, full,
@@ -539,12 +552,14 @@ __device__ void producer_role_paged(const FwdParams &p, const Shared &sh, uint32
             for (int which = 0; which < 2; ++which, ++it) {
                 const uint32_t slot = it % C::kSlots;
                 const uint32_t use = it / C::kSlots;
-                const uint32_t full = sh.kv_full0 + 8 * slot;
-                const bool skip = w == p.drop_load_item && j == item.kv0 && which == 0;   // test hook
+                // paired slots: V(j) lands on K(j)'s barrier, armed for both tiles
+                const uint32_t full = sh.kv_full0 + 8 * (C::kPairedSlots ? slot & ~1u : slot);
+                const bool skip = w == p.drop_load_item && j == item.kv0 && (C::kPairedSlots || which == 0);   // test hook
                 bool armed = true;
-                if (lane == 0) {
+                if (lane == 0 && (!C::kPairedSlots || which == 0)) {
                     armed = wait_bar(sh.kv_empty0 + 8 * slot, (use & 1) ^ 1, sh.abort_flag, 0, w, j);
-                    if (armed && !skip) ptx::mbar_arrive_expect_tx(full, C::kKVTileBytes);
+                    if (armed && !skip)
+                        ptx::mbar_arrive_expect_tx(full, (C::kPairedSlots ? 2 : 1) * C::kKVTileBytes);
                 }
                 if (!__shfl_sync(0xffffffffu, armed, 0)) {
                     ok = false;
@@ -662,7 +677,7 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
                 const int buf = (jj - kv0) & 1;
                 issue_s<D, C::kBC, F8>(tS[buf], sQ[0], ring_tile(ki));
                 ptx::mma_commit(buf ? sh.s_alt : sh.s_full0);
-                ptx::mma_commit(sh.kv_empty0 + 8 * (ki % C::kSlots));
+                if (!C::kPairedSlots) ptx::mma_commit(sh.kv_empty0 + 8 * (ki % C::kSlots));
                 return true;
             };
             if (!issue_s_buf(kv0)) return;
@@ -670,13 +685,14 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
             if (nk0 <= kv0 + 2) ptx::mma_commit(sh.q_empty);   // every S of the item issued
             for (int j = kv0; j < nk0; ++j) {
                 const uint32_t vi = b0 + 2 * (j - kv0) + 1;
-                if (!wait_bar(ring_bar(vi), (vi / C::kSlots) & 1, sh.abort_flag, 1, w, j)) return;
+                // paired slots: V(j) arrived with K(j), before S(j) was issued
+                if (!C::kPairedSlots && !wait_bar(ring_bar(vi), (vi / C::kSlots) & 1, sh.abort_flag, 1, w, j)) return;
                 if (!wait_bar(sh.p_full0, p_phase[0], sh.abort_flag, 1, w, j)) return;
                 p_phase[0] ^= 1u;
                 ptx::tc_fence_after_sync();
                 issue_pv<D, C::kBC, F8>(tO[0], tS[(j - kv0) & 1], ring_tile(vi), j > kv0);
                 ptx::mma_commit(j == nk0 - 1 ? sh.o_full0 : sh.pv_done);
-                ptx::mma_commit(sh.kv_empty0 + 8 * (vi % C::kSlots));
+                ptx::mma_commit(sh.kv_empty0 + 8 * ((C::kPairedSlots ? vi - 1 : vi) % C::kSlots));
                 if (j + 2 < nk0) {
                     if (!issue_s_buf(j + 2)) return;
                     if (j + 3 == nk0) ptx::mma_commit(sh.q_empty);
@@ -696,14 +712,17 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
                 ptx::mma_commit(sh.s_full0 + 8 * t);
             }
         }
-        ptx::mma_commit(sh.kv_empty0 + 8 * ks);
+        if (!C::kPairedSlots) ptx::mma_commit(sh.kv_empty0 + 8 * ks);
         if (nkv == kv0 + 1) ptx::mma_commit(sh.q_empty);
         ++it;
 
         for (int j = kv0; j < nkv; ++j) {
             const uint32_t vs = it % C::kSlots;
-            if (!wait_bar(sh.kv_full0 + 8 * vs, (it / C::kSlots) & 1, sh.abort_flag, 1, w, j)) return;
-            ptx::tc_fence_after_sync();
+            // paired slots: V(j) arrived with K(j), before S(j) was issued
+            if (!C::kPairedSlots) {
+                if (!wait_bar(sh.kv_full0 + 8 * vs, (it / C::kSlots) & 1, sh.abort_flag, 1, w, j)) return;
+                ptx::tc_fence_after_sync();
+            }
             ++it;
             const uint32_t v_tile = smem_ring + vs * C::kKVTileBytes;
             const bool more = j + 1 < nkv;
@@ -732,13 +751,13 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
                 issue_pv<D, C::kBC, F8>(tO[1], tS[1], v_tile, j > kv0);
                 if (j == nk1 - 1) ptx::mma_commit(sh.o_full0 + 8);
             }
-            ptx::mma_commit(sh.kv_empty0 + 8 * vs);
+            ptx::mma_commit(sh.kv_empty0 + 8 * (C::kPairedSlots ? vs - 1 : vs));   // paired: the K/V pair
             if (more) {
                 if (j + 1 < nk1) {
                     issue_s<D, C::kBC, F8>(tS[1], sQ[1], smem_ring + ks2 * C::kKVTileBytes);
                     ptx::mma_commit(sh.s_full0 + 8);
                 }
-                ptx::mma_commit(sh.kv_empty0 + 8 * ks2);
+                if (!C::kPairedSlots) ptx::mma_commit(sh.kv_empty0 + 8 * ks2);
                 if (j + 2 == nkv) ptx::mma_commit(sh.q_empty);
                 ++it;
             }
@@ -1210,7 +1229,8 @@ __global__ void __launch_bounds__(Config<D>::kThreads, Config<D>::kCtasPerSm)
             // Drain: every copy this CTA started must land before it exits.
             const uint32_t first = loads_issued > (uint32_t)C::kSlots ? loads_issued - C::kSlots : 0u;
             for (uint32_t x = first; x < loads_issued; ++x)
-                wait_drain(sh.kv_full0 + 8 * (x % C::kSlots), (x / C::kSlots) & 1);
+                if (!C::kPairedSlots || (x & 1u) == 0)   // paired: one barrier per K/V pair
+                    wait_drain(sh.kv_full0 + 8 * (x % C::kSlots), (x / C::kSlots) & 1);
             if (q_arms > 0) wait_drain(sh.q_full, (q_arms - 1) & 1);
         }
         __syncwarp();
