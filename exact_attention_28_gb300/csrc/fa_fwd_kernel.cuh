@@ -728,6 +728,14 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
             const bool more = j + 1 < nkv;
             const uint32_t ks2 = it % C::kSlots;
 
+            // Each tile's step is a cycle: softmax_t(j) -> P_t(j) V_j -> S_t(j+1)
+            // -> softmax_t(j+1).  Only MMA issues sit in it: K(j+1) is awaited
+            // before P_0(j) (this thread is idle until then anyway) and V_j's
+            // slot is released after S_1(j+1).
+            if (more) {
+                if (!wait_bar(sh.kv_full0 + 8 * ks2, (it / C::kSlots) & 1, sh.abort_flag, 1, w, j + 1))
+                    return;
+            }
             if (j < nk0) {
                 if (!wait_bar(sh.p_full0, p_phase[0], sh.abort_flag, 1, w, j)) return;
                 p_phase[0] ^= 1u;
@@ -735,14 +743,10 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
                 issue_pv<D, C::kBC, F8>(tO[0], tS[0], v_tile, j > kv0);
                 if (j == nk0 - 1) ptx::mma_commit(sh.o_full0);
             }
-            if (more) {
-                if (!wait_bar(sh.kv_full0 + 8 * ks2, (it / C::kSlots) & 1, sh.abort_flag, 1, w, j + 1))
-                    return;
-                ptx::tc_fence_after_sync();
-                if (j + 1 < nk0) {
-                    issue_s<D, C::kBC, F8>(tS[0], sQ[0], smem_ring + ks2 * C::kKVTileBytes);
-                    ptx::mma_commit(sh.s_full0);
-                }
+            ptx::tc_fence_after_sync();
+            if (more && j + 1 < nk0) {
+                issue_s<D, C::kBC, F8>(tS[0], sQ[0], smem_ring + ks2 * C::kKVTileBytes);
+                ptx::mma_commit(sh.s_full0);
             }
             if (j < nk1) {
                 if (!wait_bar(sh.p_full0 + 8, p_phase[1], sh.abort_flag, 1, w, j)) return;
@@ -751,12 +755,12 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
                 issue_pv<D, C::kBC, F8>(tO[1], tS[1], v_tile, j > kv0);
                 if (j == nk1 - 1) ptx::mma_commit(sh.o_full0 + 8);
             }
+            if (more && j + 1 < nk1) {
+                issue_s<D, C::kBC, F8>(tS[1], sQ[1], smem_ring + ks2 * C::kKVTileBytes);
+                ptx::mma_commit(sh.s_full0 + 8);
+            }
             ptx::mma_commit(sh.kv_empty0 + 8 * (C::kPairedSlots ? vs - 1 : vs));   // paired: the K/V pair
             if (more) {
-                if (j + 1 < nk1) {
-                    issue_s<D, C::kBC, F8>(tS[1], sQ[1], smem_ring + ks2 * C::kKVTileBytes);
-                    ptx::mma_commit(sh.s_full0 + 8);
-                }
                 if (!C::kPairedSlots) ptx::mma_commit(sh.kv_empty0 + 8 * ks2);
                 if (j + 2 == nkv) ptx::mma_commit(sh.q_empty);
                 ++it;
