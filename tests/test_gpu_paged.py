@@ -88,9 +88,12 @@ def test_paged_unallocated_blocks(ops, block_size):
     run_and_check(ops, q, kc, vc, table, sl, True, "holes causal")
 
 
-def test_paged_full_prefill_equals_dense_forward(ops):
+# 16-key pages are copied by the producer lanes into the swizzled tile layout
+# by hand, larger ones by TMA boxes: both must give the dense forward's bits
+@pytest.mark.parametrize("bs,d", [(128, 128), (16, 128), (16, 64), (32, 64)])
+def test_paged_full_prefill_equals_dense_forward(ops, bs, d):
     # identity table, Nq = seq_len: the paged call equals the dense causal forward
-    B, H, N, d, bs = 1, 4, 512, 128, 128
+    B, H, N = 1, 4, 512
     q, k, v = inputs.custom_inputs(21, B, H, N, N, d)
     kc = np.ascontiguousarray(k[0].reshape(H, N // bs, bs, d).transpose(1, 0, 2, 3))
     vc = np.ascontiguousarray(v[0].reshape(H, N // bs, bs, d).transpose(1, 0, 2, 3))
@@ -100,6 +103,31 @@ def test_paged_full_prefill_equals_dense_forward(ops):
     o2, l2 = ops.fa_fwd(to_dev(q), to_dev(k), to_dev(v), causal=True)
     ops.check_device_status()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("block_size", [16, 128])
+def test_paged_out_of_range_entries_read_zero_keys(ops, block_size):
+    # entries >= num_blocks read as zero keys and values: the oracle sees them
+    # as blocks of zeros appended to the cache
+    q, kc, vc, table, sl = make_case(88, [400, 333], 2, 40, 128, block_size)
+    num_blocks = kc.shape[0]
+    rng = np.random.default_rng(5)
+    table = table.copy()
+    for b, s_len in enumerate(sl):
+        used = (int(s_len) + block_size - 1) // block_size
+        for lb in rng.choice(used, size=2, replace=False):
+            table[b, lb] = num_blocks + int(rng.integers(0, 4))
+    zeros = np.zeros((4,) + kc.shape[1:], dtype=kc.dtype)
+    kc_ext, vc_ext = np.concatenate([kc, zeros]), np.concatenate([vc, zeros])
+    for causal in (False, True):
+        o, lse = ops.fa_fwd_paged(to_dev(q), to_dev(kc), to_dev(vc), torch.from_numpy(table).cuda(),
+                                  torch.from_numpy(sl).cuda(), scale=float(np.float32(1 / math.sqrt(128))),
+                                  causal=causal)
+        ops.check_device_status()
+        O_ref, L_ref = paged.paged_attention(q, kc_ext, vc_ext, table, sl, float(np.float32(1 / math.sqrt(128))), causal)
+        err = np.abs(o.float().cpu().numpy().astype(np.float64) - O_ref)
+        assert err.max() <= 2e-2 and err.mean() <= 2e-3, (block_size, causal, err.max(), err.mean())
+        assert np.abs(lse.cpu().numpy().astype(np.float64) - L_ref).max() <= 1e-3
 
 
 @pytest.mark.parametrize("num_splits", [2, 3, 8])
