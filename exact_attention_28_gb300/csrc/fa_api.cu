@@ -238,7 +238,20 @@ fa_status launch(const fa::FwdParams &p, int grid, cudaStream_t stream, bool &at
             return FA_ERR_CUDA;
         attr_done = true;
     }
-    fa::fa_fwd_kernel<D, MODE><<<grid, C::kThreads, C::kSmemBytes, stream>>>(p);
+    // Programmatic stream serialisation: the CTAs may be launched and set up
+    // (barriers, tensor memory) while the previous kernel of the stream
+    // drains; the kernel waits for it before its first global access.
+    cudaLaunchAttribute attrs[1];
+    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, fa::fa_fwd_kernel<D, MODE>, p) != cudaSuccess) return FA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -1218,6 +1218,14 @@ __global__ void __launch_bounds__(Config<D>::kThreads, Config<D>::kCtasPerSm)
     __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem = *tmem_holder;
+    // The launch lets this grid start while the previous kernel of the stream
+    // drains (programmatic dependent launch).  Nothing above touched global
+    // memory; below, every access comes after the previous kernel completed:
+    // one warp waits for it, the others at the barrier, where they issue
+    // nothing.  The grid does not release its own dependents early (a
+    // dependent grid resident beside this one's last CTAs slowed them).
+    if (threadIdx.x < 32) ptx::griddep_wait();
+    __syncthreads();
 
     uint32_t loads_issued = 0, q_arms = 0;
     if (warp < kSoftmaxWarps) {

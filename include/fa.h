@@ -67,6 +67,12 @@ typedef enum {
  * launch itself.  A wait inside the kernel that runs past its limit does not
  * hang the GPU: the kernel stops, records the fact in a device status word and
  * the outputs are undefined; fa_check_device_status() reports it.
+ *
+ * Launch: the forward kernels (fa_fwd and every entry point below that runs
+ * them) are launched with programmatic stream serialisation, so their CTAs
+ * may be set up while the previous kernel of the stream drains; each waits
+ * for that kernel to complete before its first global-memory access, so
+ * ordering on the stream is unchanged.
  */
 fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
                  int B, int H, int Nq, int Nk, int d, float scale, int causal,
