@@ -306,8 +306,8 @@ __device__ __forceinline__ void bwd_teardown(uint32_t tmem, const BwdShared &sh,
 //
 // TMEM: S^T [0,128) (P^T as bf16 pairs in [0,64)), dP^T [128,256) (dS^T in
 // [128,192)), dV [256, 256+D), dK [256+D, 256+2D).  Lane = key.
-// Warps 0-3: thread t = key j*128 + t, elementwise.  Warp 4, lane 0: loads
-// and MMAs, per query tile n:
+// Warps 0-3: thread t = key j*128 + t, elementwise.  Warp 4 (converged,
+// lane 0 issues) runs the MMAs, warp 5's lane 0 the loads; per query tile n:
 //   wait P^T(n) -> dV += P^T dO_n;  S^T(n+1) = K Q_{n+1}^T     (S^T free once P^T is read)
 //   wait dS^T(n) -> dK += dS^T Q_n; dP^T(n+1) = V dO_{n+1}^T
 // so phase A of step n+1 runs while dK(n) and dP^T(n+1) execute, and phase
@@ -361,34 +361,34 @@ __device__ void dkdv_mma_role(const BwdParams &p, const BwdShared &sh, uint32_t 
     const uint32_t sK = base, sV = base + C::kTile;
     const uint32_t sQ0 = base + 2 * C::kTile, sdO0 = base + (2 + kSlotsA) * C::kTile;
     const uint32_t tST = tmem + 0, tdPT = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
-    if (!wait_bar(sh.first, 0, sh.abort_flag, 10, blockIdx.x, -1)) return;
-    if (!wait_bar(sh.loadA0, 0, sh.abort_flag, 10, blockIdx.x, 0)) return;
+    if (!wait_bar_warp(sh.first, 0, sh.abort_flag, 10, blockIdx.x, -1)) return;
+    if (!wait_bar_warp(sh.loadA0, 0, sh.abort_flag, 10, blockIdx.x, 0)) return;
     ptx::tc_fence_after_sync();
     issue_s<D, kBC>(tST, sK, sQ0);        // S^T(0) = K Q_0^T
     ptx::mma_commit(sh.sfull);
-    if (!wait_bar(sh.loadB0, 0, sh.abort_flag, 10, blockIdx.x, 0)) return;
+    if (!wait_bar_warp(sh.loadB0, 0, sh.abort_flag, 10, blockIdx.x, 0)) return;
     ptx::tc_fence_after_sync();
     issue_s<D, kBC>(tdPT, sV, sdO0);      // dP^T(0) = V dO_0^T
     ptx::mma_commit(sh.dpfull);
     for (int n = 0; n < n_i; ++n) {
         const int a = n % kSlotsA, b = n % kSlotsB;
         const int an = (n + 1) % kSlotsA, bn = (n + 1) % kSlotsB;
-        if (!wait_bar(sh.pready, n & 1, sh.abort_flag, 11, blockIdx.x, n)) return;
+        if (!wait_bar_warp(sh.pready, n & 1, sh.abort_flag, 11, blockIdx.x, n)) return;
         ptx::tc_fence_after_sync();
         issue_pv<D, kBC>(tdV, tST, sdO0 + b * C::kTile, n > 0);    // dV += P^T dO_n
         ptx::mma_commit(sh.freeB0 + 8 * b);                   // dO_n read for the last time
         if (n + 1 < n_i) {
-            if (!wait_bar(sh.loadA0 + 8 * an, ((n + 1) / kSlotsA) & 1, sh.abort_flag, 12, blockIdx.x, n + 1)) return;
+            if (!wait_bar_warp(sh.loadA0 + 8 * an, ((n + 1) / kSlotsA) & 1, sh.abort_flag, 12, blockIdx.x, n + 1)) return;
             ptx::tc_fence_after_sync();
             issue_s<D, kBC>(tST, sK, sQ0 + an * C::kTile);         // S^T(n+1)
             ptx::mma_commit(sh.sfull);
         }
-        if (!wait_bar(sh.dsready, n & 1, sh.abort_flag, 13, blockIdx.x, n)) return;
+        if (!wait_bar_warp(sh.dsready, n & 1, sh.abort_flag, 13, blockIdx.x, n)) return;
         ptx::tc_fence_after_sync();
         issue_pv<D, kBC>(tdK, tdPT, sQ0 + a * C::kTile, n > 0);    // dK += dS^T Q_n
         ptx::mma_commit(sh.freeA0 + 8 * a);                   // Q_n read for the last time
         if (n + 1 < n_i) {
-            if (!wait_bar(sh.loadB0 + 8 * bn, ((n + 1) / kSlotsB) & 1, sh.abort_flag, 14, blockIdx.x, n + 1)) return;
+            if (!wait_bar_warp(sh.loadB0 + 8 * bn, ((n + 1) / kSlotsB) & 1, sh.abort_flag, 14, blockIdx.x, n + 1)) return;
             ptx::tc_fence_after_sync();
             issue_s<D, kBC>(tdPT, sV, sdO0 + bn * C::kTile);       // dP^T(n+1)
             ptx::mma_commit(sh.dpfull);
@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
     if (threadIdx.x < 128) {
         dkdv_elementwise_role<D>(p, sh, tmem, reinterpret_cast<float *>(base_ptr + C::kStatOffset), j, bh, i_begin,
                                  n_i);
-    } else if (threadIdx.x == 128 && n_i > 0) {
+    } else if ((threadIdx.x >> 5) == 4 && n_i > 0) {   // the whole warp, converged; lane 0 issues
         dkdv_mma_role<D>(p, sh, tmem, base, n_i);
     } else if (threadIdx.x == 160 && n_i > 0) {
         dkdv_load_role<D>(p, sh, base, j, bh, i_begin, n_i, ld);
@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
 // --------------------------------------------------------------- dQ kernel
 //
 // TMEM: S [0,128), dP [128,256) (dS as bf16 pairs in [128,192)), dQ [256, 256+D).
-// Lane = query.  Warp 4, lane 0, per key tile n:
+// Lane = query.  Warp 4 (converged, lane 0 issues), per key tile n:
 //   wait S(n) read -> S(n+1) = Q K_{n+1}^T   (S(n) is in the threads' registers)
 //   wait dS(n)     -> dQ += dS K_n;  dP(n+1) = dO V_{n+1}^T
 
@@ -523,12 +523,12 @@ __device__ void dq_mma_role(const BwdParams &p, const BwdShared &sh, uint32_t tm
     const uint32_t sQ = base, sdO = base + C::kTile;
     const uint32_t sK0 = base + 2 * C::kTile, sV0 = base + (2 + kSlotsA) * C::kTile;
     const uint32_t tS = tmem + 0, tdP = tmem + 128, tdQ = tmem + 256;
-    if (!wait_bar(sh.first, 0, sh.abort_flag, 20, blockIdx.x, -1)) return;
-    if (!wait_bar(sh.loadA0, 0, sh.abort_flag, 20, blockIdx.x, 0)) return;
+    if (!wait_bar_warp(sh.first, 0, sh.abort_flag, 20, blockIdx.x, -1)) return;
+    if (!wait_bar_warp(sh.loadA0, 0, sh.abort_flag, 20, blockIdx.x, 0)) return;
     ptx::tc_fence_after_sync();
     issue_s<D, kBC>(tS, sQ, sK0);        // S(0) = Q K_0^T
     ptx::mma_commit(sh.sfull);
-    if (!wait_bar(sh.loadB0, 0, sh.abort_flag, 20, blockIdx.x, 0)) return;
+    if (!wait_bar_warp(sh.loadB0, 0, sh.abort_flag, 20, blockIdx.x, 0)) return;
     ptx::tc_fence_after_sync();
     issue_s<D, kBC>(tdP, sdO, sV0);      // dP(0) = dO V_0^T
     ptx::mma_commit(sh.dpfull);
@@ -536,19 +536,19 @@ __device__ void dq_mma_role(const BwdParams &p, const BwdShared &sh, uint32_t tm
     for (int n = 0; n < n_j; ++n) {
         const int a = n % kSlotsA;
         const int an = (n + 1) % kSlotsA, bn = (n + 1) % kSlotsB;
-        if (!wait_bar(sh.pready, n & 1, sh.abort_flag, 21, blockIdx.x, n)) return;
+        if (!wait_bar_warp(sh.pready, n & 1, sh.abort_flag, 21, blockIdx.x, n)) return;
         if (n + 1 < n_j) {
-            if (!wait_bar(sh.loadA0 + 8 * an, ((n + 1) / kSlotsA) & 1, sh.abort_flag, 22, blockIdx.x, n + 1)) return;
+            if (!wait_bar_warp(sh.loadA0 + 8 * an, ((n + 1) / kSlotsA) & 1, sh.abort_flag, 22, blockIdx.x, n + 1)) return;
             ptx::tc_fence_after_sync();
             issue_s<D, kBC>(tS, sQ, sK0 + an * C::kTile);          // S(n+1)
             ptx::mma_commit(sh.sfull);
         }
-        if (!wait_bar(sh.dsready, n & 1, sh.abort_flag, 23, blockIdx.x, n)) return;
+        if (!wait_bar_warp(sh.dsready, n & 1, sh.abort_flag, 23, blockIdx.x, n)) return;
         ptx::tc_fence_after_sync();
         issue_pv<D, kBC>(tdQ, tdP, sK0 + a * C::kTile, n > 0);     // dQ += dS K_n
         ptx::mma_commit(sh.freeA0 + 8 * a);                   // K_n read for the last time
         if (n + 1 < n_j) {
-            if (!wait_bar(sh.loadB0 + 8 * bn, ((n + 1) / kSlotsB) & 1, sh.abort_flag, 24, blockIdx.x, n + 1)) return;
+            if (!wait_bar_warp(sh.loadB0 + 8 * bn, ((n + 1) / kSlotsB) & 1, sh.abort_flag, 24, blockIdx.x, n + 1)) return;
             ptx::tc_fence_after_sync();
             issue_s<D, kBC>(tdP, sdO, sV0 + bn * C::kTile);        // dP(n+1)
             ptx::mma_commit(sh.dpfull);
@@ -610,7 +610,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
     }
     BwdLoads ld;
     if (threadIdx.x < 128) dq_elementwise_role<D>(p, sh, tmem, i, bh, n_j);
-    else if (threadIdx.x == 128) dq_mma_role<D>(p, sh, tmem, base, n_j);
+    else if ((threadIdx.x >> 5) == 4) dq_mma_role<D>(p, sh, tmem, base, n_j);   // whole warp; lane 0 issues
     else if (threadIdx.x == 160) dq_load_role<D>(p, sh, base, i, bh, n_j, ld);
     __syncwarp();
     bwd_teardown<D>(tmem, sh, ld);

@@ -419,6 +419,13 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     return wait_slow(bar, parity, abort_flag, role, item, step);
 }
 
+// Warp-uniform bounded wait: every lane polls and all leave together, with
+// the same result (the MMA warp runs its loop converged).
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                              int role, int item, int step) {
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, role, item, step));
+}
+
 // Bounded wait used while shutting down: ignores the abort flag (copies and
 // MMAs already started must still be waited for), gives up after the limit.
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
@@ -655,7 +662,7 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
         const int kv0 = item.kv0;
         const int nk0 = item.nk[0], nk1 = item.nk[1];   // tile t is active for kv0 <= j < nk_t
         const int nkv = max(nk0, nk1);
-        if (!wait_bar(sh.q_full, k & 1, sh.abort_flag, 1, w, -1)) return;
+        if (!wait_bar_warp(sh.q_full, k & 1, sh.abort_flag, 1, w, -1)) return;
         ptx::tc_fence_after_sync();
         if (nkv <= kv0) {   // an empty key slice: release Q and move on
             ptx::mma_commit(sh.q_empty);
@@ -672,7 +679,7 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
             auto ring_tile = [&](uint32_t idx) { return smem_ring + (idx % C::kSlots) * C::kKVTileBytes; };
             auto issue_s_buf = [&](int jj) -> bool {   // S(jj) into buffer (jj - kv0) & 1
                 const uint32_t ki = b0 + 2 * (jj - kv0);
-                if (!wait_bar(ring_bar(ki), (ki / C::kSlots) & 1, sh.abort_flag, 1, w, jj)) return false;
+                if (!wait_bar_warp(ring_bar(ki), (ki / C::kSlots) & 1, sh.abort_flag, 1, w, jj)) return false;
                 ptx::tc_fence_after_sync();
                 const int buf = (jj - kv0) & 1;
                 issue_s<D, C::kBC, F8>(tS[buf], sQ[0], ring_tile(ki));
@@ -686,8 +693,8 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
             for (int j = kv0; j < nk0; ++j) {
                 const uint32_t vi = b0 + 2 * (j - kv0) + 1;
                 // paired slots: V(j) arrived with K(j), before S(j) was issued
-                if (!C::kPairedSlots && !wait_bar(ring_bar(vi), (vi / C::kSlots) & 1, sh.abort_flag, 1, w, j)) return;
-                if (!wait_bar(sh.p_full0, p_phase[0], sh.abort_flag, 1, w, j)) return;
+                if (!C::kPairedSlots && !wait_bar_warp(ring_bar(vi), (vi / C::kSlots) & 1, sh.abort_flag, 1, w, j)) return;
+                if (!wait_bar_warp(sh.p_full0, p_phase[0], sh.abort_flag, 1, w, j)) return;
                 p_phase[0] ^= 1u;
                 ptx::tc_fence_after_sync();
                 issue_pv<D, C::kBC, F8>(tO[0], tS[(j - kv0) & 1], ring_tile(vi), j > kv0);
@@ -704,7 +711,7 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
 
         // S_t(kv0) for both tiles from the first K tile.
         uint32_t ks = it % C::kSlots;
-        if (!wait_bar(sh.kv_full0 + 8 * ks, (it / C::kSlots) & 1, sh.abort_flag, 1, w, kv0)) return;
+        if (!wait_bar_warp(sh.kv_full0 + 8 * ks, (it / C::kSlots) & 1, sh.abort_flag, 1, w, kv0)) return;
         ptx::tc_fence_after_sync();
         for (int t = 0; t < 2; ++t) {
             if (item.nk[t] > kv0) {
@@ -720,7 +727,7 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
             const uint32_t vs = it % C::kSlots;
             // paired slots: V(j) arrived with K(j), before S(j) was issued
             if (!C::kPairedSlots) {
-                if (!wait_bar(sh.kv_full0 + 8 * vs, (it / C::kSlots) & 1, sh.abort_flag, 1, w, j)) return;
+                if (!wait_bar_warp(sh.kv_full0 + 8 * vs, (it / C::kSlots) & 1, sh.abort_flag, 1, w, j)) return;
                 ptx::tc_fence_after_sync();
             }
             ++it;
@@ -733,11 +740,11 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
             // before P_0(j) (this thread is idle until then anyway) and V_j's
             // slot is released after S_1(j+1).
             if (more) {
-                if (!wait_bar(sh.kv_full0 + 8 * ks2, (it / C::kSlots) & 1, sh.abort_flag, 1, w, j + 1))
+                if (!wait_bar_warp(sh.kv_full0 + 8 * ks2, (it / C::kSlots) & 1, sh.abort_flag, 1, w, j + 1))
                     return;
             }
             if (j < nk0) {
-                if (!wait_bar(sh.p_full0, p_phase[0], sh.abort_flag, 1, w, j)) return;
+                if (!wait_bar_warp(sh.p_full0, p_phase[0], sh.abort_flag, 1, w, j)) return;
                 p_phase[0] ^= 1u;
                 ptx::tc_fence_after_sync();
                 issue_pv<D, C::kBC, F8>(tO[0], tS[0], v_tile, j > kv0);
@@ -749,7 +756,7 @@ __device__ void mma_role(const FwdParams &p, const Shared &sh, uint32_t tmem, ui
                 ptx::mma_commit(sh.s_full0);
             }
             if (j < nk1) {
-                if (!wait_bar(sh.p_full0 + 8, p_phase[1], sh.abort_flag, 1, w, j)) return;
+                if (!wait_bar_warp(sh.p_full0 + 8, p_phase[1], sh.abort_flag, 1, w, j)) return;
                 p_phase[1] ^= 1u;
                 ptx::tc_fence_after_sync();
                 issue_pv<D, C::kBC, F8>(tO[1], tS[1], v_tile, j > kv0);
@@ -1248,7 +1255,8 @@ __global__ void __launch_bounds__(Config<D>::kThreads, Config<D>::kCtasPerSm)
         __syncwarp();
     } else {
         if constexpr (C::kRegSplit) ptx::setmaxnreg_dec<kOtherRegs>();
-        if (warp == kMmaWarp && lane == 0) mma_role<D, MODE>(p, sh, tmem, smem_q, smem_ring);
+        // the whole warp, converged: uniform descriptor arithmetic; lane 0 issues
+        if (warp == kMmaWarp) mma_role<D, MODE>(p, sh, tmem, smem_q, smem_ring);
         __syncwarp();
     }
 
