@@ -67,6 +67,7 @@ CALLS = [
     (1, 3, 300, 1500, 64, True, 8, 202),       # early query tiles: 6 of 8 key slices empty
     (1, 3, 300, 1500, 64, True, 8, 303),       # the same shape again, other inputs
     (1, 32, 1, 32768, 128, False, 0, 404),     # a decode shape; the library picks the slice count
+    (2, 4, 200, 600, 64, True, 1, 606),         # one slice: no partials, the scratch area is not used
 ]
 
 
