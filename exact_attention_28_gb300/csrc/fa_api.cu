@@ -37,38 +37,81 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// Every map of this library: 128-byte swizzle, 256-byte L2 promotion, no
+// interleave, zero fill, unit element strides.  Encoded maps are kept in a
+// small per-thread cache keyed by everything that goes into the encoding
+// (element type, rank, address, sizes, strides, box), so a repeated call on
+// the same buffers and shapes skips the driver call; a hit returns exactly the
+// map the driver would encode again, whatever else changed in between.
+bool encode_cached(CUtensorMap *map, CUtensorMapDataType type, int rank, const void *ptr, const cuuint64_t *dims,
+                   const cuuint64_t *strides, const cuuint32_t *box) {
+    struct Entry {
+        bool used;
+        CUtensorMapDataType type;
+        int rank;
+        const void *ptr;
+        cuuint64_t dims[4], strides[3];
+        cuuint32_t box[4];
+        CUtensorMap map;
+    };
+    constexpr int kEntries = 32;
+    thread_local Entry cache[kEntries] = {};
+    thread_local int next = 0;
+    for (Entry &e : cache) {
+        if (!e.used || e.type != type || e.rank != rank || e.ptr != ptr) continue;
+        bool same = true;
+        for (int i = 0; i < rank; ++i) same = same && e.dims[i] == dims[i] && e.box[i] == box[i];
+        for (int i = 0; i + 1 < rank; ++i) same = same && e.strides[i] == strides[i];
+        if (same) {
+            *map = e.map;
+            return true;
+        }
+    }
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (fn(map, type, static_cast<cuuint32_t>(rank), const_cast<void *>(ptr), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    Entry &e = cache[next];
+    next = (next + 1) % kEntries;
+    e = Entry{};
+    e.used = true;
+    e.type = type;
+    e.rank = rank;
+    e.ptr = ptr;
+    for (int i = 0; i < rank; ++i) {
+        e.dims[i] = dims[i];
+        e.box[i] = box[i];
+    }
+    for (int i = 0; i + 1 < rank; ++i) e.strides[i] = strides[i];
+    e.map = *map;
+    return true;
+}
+
 // [BH][N][d] bf16, boxes of 64 columns x box_rows rows x 1 head, 128-byte
 // swizzle.  Rows past N inside a head read as zero (the map is 3-D, so a box
 // never spills into the next head).
 bool make_map(CUtensorMap *map, const void *ptr, int64_t BH, int64_t N, int d, int box_rows = fa::kBR) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                                 static_cast<cuuint64_t>(BH)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
     const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_cached(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box);
 }
 
 // Paged cache [num_blocks][H][block_size][d] bf16, boxes of 64 columns x
 // min(block_size, keys per K/V tile) rows of one head of one block, 128-byte
 // swizzle.
 bool make_map_paged(CUtensorMap *map, const void *ptr, int num_blocks, int H, int block_size, int d) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(block_size),
                                 static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(num_blocks)};
     const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(block_size) * d * 2,
                                    static_cast<cuuint64_t>(H) * block_size * d * 2};
     const int bc = fa::kv_tile_keys(d);
     const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(block_size < bc ? block_size : bc), 1, 1};
-    const cuuint32_t estr[4] = {1, 1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_cached(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, dims, strides, box);
 }
 
 // 8-bit [BH][rows][inner] (inner bytes per row, a multiple of 16), boxes of
@@ -76,16 +119,11 @@ bool make_map_paged(CUtensorMap *map, const void *ptr, int num_blocks, int H, in
 // ([BH][N][128], box 128 x 128) and V^T ([BH][128][ldn], box 128 keys x 128
 // channels).
 bool make_map_u8(CUtensorMap *map, const void *ptr, int64_t BH, int64_t rows, int64_t inner, int box_rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
                                 static_cast<cuuint64_t>(BH)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows) * inner};
     const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(box_rows), 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_cached(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, ptr, dims, strides, box);
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
